@@ -1,0 +1,137 @@
+"""Seeded synthetic workloads for grouped-query attention.
+
+This module only draws random numbers and fixes shapes; it holds none of the
+attention arithmetic.  Both the CUDA path's tests/benchmark and the oracle's
+tests take their inputs from here, so the two always see the same values.
+
+Recipe: ``torch.Generator('cpu').manual_seed(seed)``; draws in the order Q,
+K, V, then key lengths; values are ``randn`` in float32, cast to bfloat16 by
+round-to-nearest-even for bf16 workloads; lengths are ``randint(lo, hi+1)``.
+The workloads stand in for the pages' BERT-base seq-1024 encoder, a
+BERT-large long-document encoder, a Llama-style 64/8-head decode step and a
+long causal prefill; no dataset is used.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional, Tuple
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class PrefillWorkload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Sk: int
+    D: int
+    causal: bool
+    lens: Optional[Tuple[int, int]]  # key lengths ~ U[lo, hi] per batch entry, None = full
+    dtype: str                       # "bf16" or "fp32"
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeWorkload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    Smax: int
+    lens: Tuple[int, int]            # cached lengths ~ U[lo, hi]
+    dtype: str
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
+WORKLOADS = {
+    # tiny fp32 check case: B=1 Hq=4 Hkv=2 S=64 D=64, no padding
+    "tiny": PrefillWorkload("tiny", 1, 4, 2, 64, 64, 64, False, None, "fp32", 0),
+    # BERT-base-shaped encoder attention, key padding U[512,1024]
+    "bert_base": PrefillWorkload("bert_base", 32, 12, 3, 1024, 1024, 64, False, (512, 1024),
+                                 "bf16", 1),
+    # BERT-large-shaped long-document encoder attention, full length
+    "bert_large_long": PrefillWorkload("bert_large_long", 8, 24, 4, 4096, 4096, 64, False, None,
+                                       "bf16", 2),
+    # Llama-style 64/8-head decode over a cache with lengths U[1024,8192]
+    "llama_decode": DecodeWorkload("llama_decode", 64, 64, 8, 128, 8192, (1024, 8192), "bf16", 3),
+    # long causal prefill, D=128
+    "causal_long": PrefillWorkload("causal_long", 4, 32, 8, 8192, 8192, 128, True, None, "bf16", 4),
+}
+
+
+def _cast(x: torch.Tensor, dtype: str) -> torch.Tensor:
+    if dtype == "bf16":
+        return x.to(torch.bfloat16)
+    if dtype == "fp32":
+        return x
+    raise ValueError("dtype must be 'bf16' or 'fp32'")
+
+
+def make_prefill(B, Hq, Hkv, Sq, Sk, D, *, seed=0, lens=None, dtype="bf16", q_mult=1.0):
+    """Return dict(q [B,Sq,Hq,D], k, v [B,Sk,Hkv,D], seqlens_k int32 [B] or None) on the CPU.
+
+    ``q_mult`` multiplies Q before the cast (a "peaky" variant whose softmax
+    is concentrated on few keys).
+    """
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    q = torch.randn((B, Sq, Hq, D), generator=g, dtype=torch.float32)
+    k = torch.randn((B, Sk, Hkv, D), generator=g, dtype=torch.float32)
+    v = torch.randn((B, Sk, Hkv, D), generator=g, dtype=torch.float32)
+    seqlens = None
+    if lens is not None:
+        lo, hi = lens
+        seqlens = torch.randint(int(lo), int(hi) + 1, (B,), generator=g, dtype=torch.int64)
+        seqlens = seqlens.to(torch.int32)
+    if q_mult != 1.0:
+        q = q * float(q_mult)
+    return dict(q=_cast(q, dtype), k=_cast(k, dtype), v=_cast(v, dtype), seqlens_k=seqlens)
+
+
+def make_decode(B, Hq, Hkv, D, Smax, *, seed=0, lens=(1, None), dtype="bf16"):
+    """Return dict(q [B,Hq,D], kcache, vcache [B,Smax,Hkv,D], cache_seqlens int32 [B])."""
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    q = torch.randn((B, Hq, D), generator=g, dtype=torch.float32)
+    kc = torch.randn((B, Smax, Hkv, D), generator=g, dtype=torch.float32)
+    vc = torch.randn((B, Smax, Hkv, D), generator=g, dtype=torch.float32)
+    lo, hi = lens
+    hi = Smax if hi is None else hi
+    seqlens = torch.randint(int(lo), int(hi) + 1, (B,), generator=g, dtype=torch.int64)
+    return dict(q=_cast(q, dtype), kcache=_cast(kc, dtype), vcache=_cast(vc, dtype),
+                cache_seqlens=seqlens.to(torch.int32))
+
+
+def make_workload(w, seed=None):
+    """Inputs of a named workload (a key of WORKLOADS or a workload object)."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    s = w.seed if seed is None else seed
+    if isinstance(w, DecodeWorkload):
+        return make_decode(w.B, w.Hq, w.Hkv, w.D, w.Smax, seed=s, lens=w.lens, dtype=w.dtype)
+    return make_prefill(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, seed=s, lens=w.lens, dtype=w.dtype)
+
+
+def sample_rows(n_total: int, n: int, seed: int, must=()) -> torch.Tensor:
+    """Deterministic sorted sample of ``n`` distinct row ids in [0, n_total), including ``must``."""
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    picked = set(int(m) for m in must if 0 <= int(m) < n_total)
+    if n >= n_total:
+        return torch.arange(n_total, dtype=torch.int64)
+    perm = torch.randperm(n_total, generator=g)[: n + len(picked)].tolist()
+    for r in perm:
+        if len(picked) >= n:
+            break
+        picked.add(int(r))
+    return torch.tensor(sorted(picked), dtype=torch.int64)

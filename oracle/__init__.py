@@ -1,0 +1,120 @@
+"""fp64 CPU oracle for grouped-query attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product library
+(``grouped_query_attention_08_b300``) never imports it and shares no code
+with it; both sides only share the seeded input generators.
+
+``oracle.c`` holds the definition (plain two-pass softmax in fp64, one row at
+a time); this module compiles it with gcc on first use and wraps it with
+ctypes.  ``brute.py`` is an independent pure-Python restatement used to pin
+the C code on tiny inputs.
+
+Sources: see the header of ``oracle.c`` (pages "3个GQA核心优化技巧" on
+blog.gitcode.com, the GQA paper summary on azimuth.plus, the aifullclass.xyz
+BERT attention article, and "FlashAttention Serisi" on webturing.pages.dev).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into liboracle.so (gcc, -O2, OpenMP, no fast-math)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + ".tmp%d" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+                               "-fno-fast-math", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i32, i64, dbl, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+            lib.oracle_gqa_attention.restype = i32
+            lib.oracle_gqa_attention.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                 i32, i32, dbl, i32, vp, vp, i64]
+            _lib = lib
+    return _lib
+
+
+def _f32(a) -> np.ndarray:
+    if hasattr(a, "detach"):  # torch tensor: widen exactly to float32 on the CPU
+        a = a.detach().to("cpu").float().numpy()
+    return np.ascontiguousarray(a, dtype=np.float32)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def attention(q, k, v, *, scale=None, causal=False, seqlens_k=None, rows=None, sk=None):
+    """Oracle GQA attention.
+
+    q [B,Sq,Hq,D]; k,v [B,Skcap,Hkv,D] (float arrays or CPU tensors holding the
+    exact input values); ``sk`` = logical key count (default Skcap);
+    ``seqlens_k`` int [B] or None; ``rows`` optional int64 array of
+    (b*Hq+h)*Sq+i row ids.  Returns (out, lse) in float64: out [B,Sq,Hq,D] and
+    lse [B,Hq,Sq], or out [nrows,D] and lse [nrows] when ``rows`` is given.
+    ``scale`` defaults to 1/sqrt(D) ([GQA-BERT] "阶段二").
+    """
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    B, Sq, Hq, D = q.shape
+    Bk, Skcap, Hkv, Dk = k.shape
+    if Bk != B or Dk != D or v.shape != k.shape:
+        raise ValueError("shape mismatch")
+    Sk = Skcap if sk is None else int(sk)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lens = None
+    if seqlens_k is not None:
+        if hasattr(seqlens_k, "detach"):
+            seqlens_k = seqlens_k.detach().cpu().numpy()
+        lens = np.ascontiguousarray(seqlens_k, dtype=np.int32)
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        out = np.zeros((rows.shape[0], D), np.float64)
+        lse = np.zeros((rows.shape[0],), np.float64)
+    else:
+        out = np.zeros((B, Sq, Hq, D), np.float64)
+        lse = np.zeros((B, Hq, Sq), np.float64)
+    lib = _load()
+    rc = lib.oracle_gqa_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse),
+                                  B, Hq, Hkv, Sq, Sk, Skcap, D, float(scale), int(bool(causal)),
+                                  _ptr(lens) if lens is not None else None,
+                                  _ptr(rows) if rows is not None else None,
+                                  0 if rows is None else rows.shape[0])
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments (code %d)" % rc)
+    return out, lse
+
+
+def decode(q, kcache, vcache, cache_seqlens, *, scale=None, rows=None):
+    """Oracle single-token decode: q [B,Hq,D]; caches [B,Smax,Hkv,D].
+
+    The new token attends to cache rows [0, cache_seqlens[b]) with no causal
+    term.  Returns (out [B,Hq,D], lse [B,Hq]) in float64.
+    """
+    q = _f32(q)
+    B, Hq, D = q.shape
+    out, lse = attention(q.reshape(B, 1, Hq, D), kcache, vcache, scale=scale, causal=False,
+                         seqlens_k=cache_seqlens, rows=rows)
+    if rows is not None:
+        return out, lse
+    return out.reshape(B, Hq, D), lse.reshape(B, Hq)

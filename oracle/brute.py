@@ -1,0 +1,55 @@
+"""Pure-Python brute-force GQA attention -- TEST INFRASTRUCTURE ONLY.
+
+An independent restatement of the oracle's definition with nested Python
+lists, ``math.fsum`` and ``math.exp`` (no numpy, no C).  It is used only on
+tiny shapes to pin ``oracle.c``.  Its steps follow the plain softmax
+attention written on the aifullclass.xyz BERT attention article (scores =
+q.k * scale, masked keys dropped, softmax over keys, weighted sum of V) with
+the head-to-group map of "3个GQA核心优化技巧" (blog.gitcode.com, section
+"Flash-Attention的稀疏分组优化": kv head = query head // group size).
+
+Where the C oracle takes the maximum and normalises in two passes, this one
+exponentiates every admissible score against its own maximum computed by
+``max()`` over a list, then divides each weight by an ``fsum`` of them; the
+output component is an ``fsum`` of products.
+"""
+from __future__ import annotations
+
+import math
+
+
+def attention(q, k, v, scale, causal=False, seqlens_k=None):
+    """q[b][i][h][d], k[b][j][g][d], v[b][j][g][d] nested lists of floats.
+
+    Returns (out[b][i][h][d], lse[b][h][i]) as nested lists of floats.
+    """
+    B = len(q)
+    Sq = len(q[0])
+    Hq = len(q[0][0])
+    D = len(q[0][0][0])
+    Sk = len(k[0])
+    Hkv = len(k[0][0])
+    if Hq % Hkv:
+        raise ValueError("Hq must be divisible by Hkv")
+    group = Hq // Hkv
+    out = [[[[0.0] * D for _ in range(Hq)] for _ in range(Sq)] for _ in range(B)]
+    lse = [[[0.0] * Sq for _ in range(Hq)] for _ in range(B)]
+    for b in range(B):
+        length = Sk if seqlens_k is None else int(seqlens_k[b])
+        for i in range(Sq):
+            for h in range(Hq):
+                g = h // group
+                keys = [j for j in range(length) if (not causal) or j <= i + Sk - Sq]
+                if not keys:
+                    lse[b][h][i] = -math.inf
+                    continue
+                scores = [scale * math.fsum(q[b][i][h][d] * k[b][j][g][d] for d in range(D))
+                          for j in keys]
+                top = max(scores)
+                weights = [math.exp(s - top) for s in scores]
+                total = math.fsum(weights)
+                probs = [w / total for w in weights]
+                for d in range(D):
+                    out[b][i][h][d] = math.fsum(p * v[b][j][g][d] for p, j in zip(probs, keys))
+                lse[b][h][i] = top + math.log(total)
+    return out, lse
