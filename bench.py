@@ -1,0 +1,400 @@
+#!/usr/bin/env python3
+"""Benchmark of the grouped-query attention forward on B300.
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+a prefill call (gqa_fwd) on the BERT-base-shaped encoder workload (B=32,
+Hq=12, Hkv=3, S=1024, D=64, key lengths U[512,1024]) followed by a decode
+call (gqa_decode, split-KV + combine) on the Llama-style decode workload
+(B=64, Hq=64, Hkv=8, D=128, cache lengths U[1024,8192]).  The headline
+``value`` is prefill TFLOP/s (algorithmic flops / prefill kernel time); the
+``decode`` object carries KV-cache GB/s.  Inputs are resident in HBM; between
+timed steps a 256 MB buffer is written to flush L2, and the decode step
+streams 1.2 GB of cache anyway.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--prefill WORKLOAD] [--no-cpu-baseline]
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(no collective on the data path; weak scaling); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from grouped_query_attention_08_b300 import inputs, roofline  # noqa: E402
+
+METRIC = "GQA prefill TFLOP/s & decode KV-cache GB/s on 1 B300, % of roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM traffic per launch from one ncu capture, valid only while the kernel
+# source is unchanged (sha256 of the file below).  Filled from the committed
+# profiles/*.md summaries; None = not captured for the current source.
+NCU_TRAFFIC = {
+    "prefill": {"source": "grouped_query_attention_08_b300/csrc/prefill_sm103.cuh", "sha256": None,
+                "workload": "bert_base", "bytes": None},
+    "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh", "sha256": None,
+               "workload": "llama_decode", "bytes": None},
+}
+
+
+def _sha(path):
+    with open(os.path.join(ROOT, path), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def _traffic(kind):
+    t = NCU_TRAFFIC[kind]
+    if t["bytes"] is None or t["sha256"] is None:
+        return None
+    return t["bytes"] if _sha(t["source"]) == t["sha256"] else None
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed region runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(workload, seconds=10.0):
+    """Time the fp64 oracle (as it stands) on a bounded row sample of the workload."""
+    import oracle
+    w = inputs.WORKLOADS[workload]
+    inp = inputs.make_workload(w)
+    q = inp["q"].float().numpy()
+    k = inp["k"].float().numpy()
+    v = inp["v"].float().numpy()
+    lens = None if inp["seqlens_k"] is None else inp["seqlens_k"].numpy()
+    total = w.B * w.Hq * w.Sq
+    oracle.build()
+
+    def run(n):
+        rows = inputs.sample_rows(total, n, 12345).numpy()
+        t0 = time.perf_counter()
+        oracle.attention(q, k, v, scale=w.scale, causal=w.causal, seqlens_k=lens, rows=rows)
+        dt = time.perf_counter() - t0
+        pairs = 0
+        for r in rows:
+            i = r % w.Sq
+            b = r // (w.Sq * w.Hq)
+            Lb = w.Sk if lens is None else int(lens[b])
+            lim = min(Lb, i + w.Sk - w.Sq + 1) if w.causal else Lb
+            pairs += max(0, lim)
+        return dt, 4 * w.D * pairs
+
+    dt, _ = run(256)
+    n = int(min(total, max(256, 256 * seconds / max(dt, 1e-3))))
+    dt, flops = run(n)
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": "%d of %d query rows of %s (fp64, OpenMP), %.1f s" % (n, total, workload, dt),
+            "seconds": dt}
+
+
+def run_reference(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    w = inputs.WORKLOADS[args.prefill]
+    res = []
+    for _ in range(args.warmup):
+        cpu_baseline(args.prefill, seconds=2.0)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        res.append(cpu_baseline(args.prefill, seconds=5.0))
+    wall = time.perf_counter() - t0
+    val = statistics.median([r["value"] for r in res])
+    cb = dict(res[-1])
+    cb["value"] = val
+    cb.pop("seconds", None)
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": _workload_name(w), "sampled": True},
+            "cpu_baseline": cb,
+            "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def _workload_name(w):
+    lens = "full" if w.lens is None else "U[%d,%d]" % w.lens
+    return "%s prefill B%d Hq%d Hkv%d Sq%d Sk%d D%d %s keys %s" % (
+        w.name, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, "causal" if w.causal else "non-causal", lens)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--prefill", default="bert_base",
+                    choices=["bert_base", "bert_large_long", "causal_long"])
+    ap.add_argument("--decode", default="llama_decode")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import grouped_query_attention_08_b300 as gqa
+    ws, rank, local = _dist()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    gqa.load_library()
+
+    wp = inputs.WORKLOADS[args.prefill]
+    wd = inputs.WORKLOADS[args.decode]
+    pin = inputs.make_workload(wp)
+    din = inputs.make_workload(wd)
+    P = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in pin.items()}
+    Dd = {k: v.to(device) for k, v in din.items()}
+    lens_p = None if pin["seqlens_k"] is None else pin["seqlens_k"].tolist()
+    flops_p = roofline.prefill_flops(wp.B, wp.Hq, wp.Sq, wp.Sk, wp.D, wp.causal, lens_p)
+    bytes_p = roofline.prefill_bytes(wp.B, wp.Hq, wp.Hkv, wp.Sq, wp.Sk, wp.D, lens_p)
+    lens_d = din["cache_seqlens"].tolist()
+    kv_bytes_d = roofline.decode_kv_bytes(wd.Hkv, wd.D, lens_d)
+    bytes_d = roofline.decode_bytes(wd.B, wd.Hq, wd.Hkv, wd.D, lens_d)
+
+    out_p = torch.empty_like(P["q"])
+    lse_p = torch.empty((wp.B, wp.Hq, wp.Sq), dtype=torch.float32, device=device)
+    out_d = torch.empty_like(Dd["q"])
+    nsplit = gqa.gqa_decode_num_splits(wd.B, wd.Hkv, wd.Smax, 0)
+    wsb = gqa.gqa_decode_workspace_bytes(wd.B, wd.Hq, wd.Hkv, wd.D, 0, wd.Smax)
+    work = torch.empty((max(wsb, 16),), dtype=torch.uint8, device=device)
+    flush = torch.empty((256 << 20,), dtype=torch.uint8, device=device)
+
+    def prefill():
+        gqa.gqa_fwd(P["q"], P["k"], P["v"], causal=wp.causal, seqlens_k=P["seqlens_k"], scale=wp.scale,
+                    out=out_p, lse=lse_p)
+
+    def decode():
+        gqa.gqa_decode(Dd["q"], Dd["kcache"], Dd["vcache"], Dd["cache_seqlens"], scale=wd.scale,
+                       num_splits=0, out=out_d, workspace=work)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        prefill()
+        decode()
+    torch.cuda.synchronize()
+    if gqa.gqa_device_status() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        _barrier(ws)
+        torch.cuda.synchronize()
+        t_start.record()
+        for i in range(K):
+            flush.fill_(i & 0xFF)
+            ev[i][0].record()
+            prefill()
+            ev[i][1].record()
+            decode()
+            ev[i][2].record()
+        t_end.record()
+        torch.cuda.synchronize()
+        _barrier(ws)
+    clk = clocks.summary()
+    if gqa.gqa_device_status() != 0:
+        raise RuntimeError("device error in the timed region")
+    t_pre = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    t_dec = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    total_ms = t_start.elapsed_time(t_end)
+    pre_s = _max_over_ranks(sum(t_pre) / 1e3, ws, device)
+    dec_s = _max_over_ranks(sum(t_dec) / 1e3, ws, device)
+    total_s = _max_over_ranks(total_ms / 1e3, ws, device)
+
+    value = flops_p * K * ws / pre_s / 1e12
+    dec_gbs = kv_bytes_d * K * ws / dec_s / 1e9
+    peaks, psrc = _peaks()
+    pre_avg = pre_s / K
+    dec_avg = dec_s / K
+    pre_ach = flops_p / pre_avg / 1e12
+    dec_ach = bytes_d / dec_avg / 1e9
+    tr_p, tr_d = _traffic("prefill"), _traffic("decode")
+    roof_p = {"bound": "tensor", "achieved": pre_ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+              "frac": pre_ach / peaks["bf16_tflops"], "traffic": tr_p,
+              "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % psrc if psrc == "measured" else
+              "fallback 1.8 PFLOP/s bf16",
+              "frac_of_sustained": pre_ach / peaks.get("bf16_tflops_sustained", 1400.0),
+              "algorithmic_flops_per_launch": flops_p, "kernel": "prefill_kernel<64>" if wp.D == 64 else
+              "prefill_kernel<128>"}
+    roof_d = {"bound": "hbm", "achieved": dec_ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+              "frac": dec_ach / peaks["hbm_gbs"], "traffic": tr_d,
+              "algorithmic_bytes_per_launch": bytes_d, "kernels": "decode_split_kernel + combine_kernel"}
+
+    # ---- end to end through the public API with host buffers (prefill)
+    e2e = None
+    if rank == 0 or ws > 1:
+        hq = pin["q"].pin_memory()
+        hk = pin["k"].pin_memory()
+        hv = pin["v"].pin_memory()
+        hl = None if pin["seqlens_k"] is None else pin["seqlens_k"].pin_memory()
+        ho = torch.empty(out_p.shape, dtype=out_p.dtype).pin_memory()
+        hlse = torch.empty(lse_p.shape, dtype=torch.float32).pin_memory()
+        dq, dk, dv = torch.empty_like(P["q"]), torch.empty_like(P["k"]), torch.empty_like(P["v"])
+        dl = None if hl is None else torch.empty_like(P["seqlens_k"])
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hl) if t is not None)
+        d2h = ho.numel() * ho.element_size() + hlse.numel() * 4
+
+        def e2e_step():
+            dq.copy_(hq, non_blocking=True)
+            dk.copy_(hk, non_blocking=True)
+            dv.copy_(hv, non_blocking=True)
+            if dl is not None:
+                dl.copy_(hl, non_blocking=True)
+            gqa.gqa_fwd(dq, dk, dv, causal=wp.causal, seqlens_k=dl, scale=wp.scale, out=out_p, lse=lse_p)
+            ho.copy_(out_p, non_blocking=True)
+            hlse.copy_(lse_p, non_blocking=True)
+
+        for _ in range(3):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _barrier(ws)
+        a.record()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        b.record()
+        torch.cuda.synchronize()
+        e2e_s = _max_over_ranks(a.elapsed_time(b) / 1e3, ws, device)
+        e2e = {"value": flops_p * args.e2e_steps * ws / e2e_s / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "what": "prefill through gqa_fwd with pinned host inputs copied in and out every step"}
+
+    cb = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cb = cpu_baseline(args.prefill)
+        cb.pop("seconds", None)
+
+    launches_per_step = 1 + 1 + (1 if nsplit > 1 else 0)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": K,
+            "warmup": args.warmup, "ms_per_step": total_s * 1e3 / K, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": _workload_name(wp) + " + " + (
+                "%s decode B%d Hq%d Hkv%d D%d Smax%d cache lengths U[%d,%d]" % (
+                    wd.name, wd.B, wd.Hq, wd.Hkv, wd.D, wd.Smax, wd.lens[0], wd.lens[1])),
+                "l2": "256 MB L2 flush before every step; decode inputs (2.1 GB caches) exceed L2",
+                "parallelism": "replicas" if ws > 1 else "single GPU",
+                "prefill_ms": pre_avg * 1e3, "decode_ms": dec_avg * 1e3, "decode_num_splits": nsplit},
+            "roofline": roof_p,
+            "decode": {"value": dec_gbs, "unit": "GB/s (KV-cache bytes read / decode time)",
+                       "roofline": roof_d, "kv_bytes_per_step": kv_bytes_d},
+            "clocks": clk,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * K,
+            "cpu_baseline": cb,
+        }
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

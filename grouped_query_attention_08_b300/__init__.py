@@ -1,0 +1,210 @@
+"""grouped_query_attention_08_b300 -- Python binding of libgqa (B300 / sm_103a).
+
+Thin ctypes layer over the C ABI declared in ``include/gqa.h``: it checks
+shapes and dtypes, allocates outputs with torch (device memory and streams
+are the only things torch is used for) and passes raw device pointers and the
+current CUDA stream.  Every step of the attention runs in libgqa's kernels;
+there is no CPU or PyTorch fallback -- if the library is missing the calls
+raise.
+
+Functions keep the C names:
+  gqa_fwd(q, k, v, *, causal=False, seqlens_k=None, scale=None, out=None, lse=None, return_lse=True)
+  gqa_decode(q, kcache, vcache, cache_seqlens, *, scale=None, num_splits=0, out=None, workspace=None)
+  gqa_decode_num_splits(B, Hkv, max_seqlen_k, num_splits)
+  gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, max_seqlen_k)
+  gqa_device_status(stream=None)
+  gqa_status_string(status)
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+GQA_OK = 0
+GQA_ERR_INVALID_ARG = 1
+GQA_ERR_UNSUPPORTED = 2
+GQA_ERR_CUDA = 3
+GQA_ERR_DEVICE_TIMEOUT = 4
+GQA_ERR_DEVICE_BOUNDS = 5
+GQA_DTYPE_BF16 = 0
+GQA_DTYPE_FP32 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libgqa.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class GQAError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        super().__init__("%s%s" % (gqa_status_string(status), (": " + what) if what else ""))
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Load libgqa.so (built in-tree by ``build.build()``); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError("libgqa.so is not built (%s); run grouped_query_attention_08_b300.build.build()"
+                               % _LIB_PATH)
+        lib = ctypes.CDLL(_LIB_PATH)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.gqa_fwd.restype = i32
+        lib.gqa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, i32, vp]
+        lib.gqa_decode.restype = i32
+        lib.gqa_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, vp, sz, vp]
+        lib.gqa_decode_num_splits.restype = i32
+        lib.gqa_decode_num_splits.argtypes = [i32, i32, i32, i32]
+        lib.gqa_decode_workspace_bytes.restype = sz
+        lib.gqa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.gqa_device_status.restype = i32
+        lib.gqa_device_status.argtypes = [vp]
+        lib.gqa_status_string.restype = ctypes.c_char_p
+        lib.gqa_status_string.argtypes = [i32]
+        _lib = lib
+        return lib
+
+
+def gqa_status_string(status: int) -> str:
+    try:
+        return load_library().gqa_status_string(int(status)).decode()
+    except RuntimeError:
+        return "status %d" % int(status)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return GQA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return GQA_DTYPE_FP32
+    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device, stream=None):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_cuda(*ts):
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("all tensors must be CUDA tensors (libgqa has no CPU path)")
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError("all tensors must be on the same device")
+    return dev
+
+
+def gqa_fwd(q, k, v, *, causal=False, seqlens_k=None, scale=None, out=None, lse=None,
+            return_lse=True, stream=None):
+    """Prefill / encoder GQA attention.  q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D] (bf16 or fp32, CUDA).
+
+    Returns (out [B,Sq,Hq,D], lse [B,Hq,Sq] fp32 or None).  ``scale`` defaults to
+    1/sqrt(D); ``seqlens_k`` is an int32 CUDA tensor [B] of key lengths.
+    """
+    torch = _torch()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, S, H, D]")
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between q, k and v")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    code = _dtype_code(q)
+    if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or tuple(seqlens_k.shape) != (B,)):
+        raise ValueError("seqlens_k must be int32 [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    dev = _check_cuda(q, k, v, out, lse, seqlens_k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = load_library().gqa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                                float(scale), int(bool(causal)), _ptr(seqlens_k), code,
+                                _stream(dev, stream))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_fwd")
+    return out, lse
+
+
+def gqa_decode_num_splits(B, Hkv, max_seqlen_k, num_splits=0) -> int:
+    n = load_library().gqa_decode_num_splits(int(B), int(Hkv), int(max_seqlen_k), int(num_splits))
+    if n < 0:
+        raise GQAError(-n, "gqa_decode_num_splits")
+    return n
+
+
+def gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, max_seqlen_k) -> int:
+    return int(load_library().gqa_decode_workspace_bytes(int(B), int(Hq), int(Hkv), int(D),
+                                                         int(num_splits), int(max_seqlen_k)))
+
+
+def gqa_decode(q, kcache, vcache, cache_seqlens, *, scale=None, num_splits=0, out=None,
+               workspace=None, stream=None):
+    """Single-token decode.  q [B,Hq,D]; caches [B,Smax,Hkv,D]; cache_seqlens int32 [B].
+
+    Returns out [B,Hq,D].  ``workspace`` (uint8 CUDA tensor) is allocated when not given.
+    """
+    torch = _torch()
+    if q.dim() != 3 or kcache.dim() != 4 or vcache.dim() != 4:
+        raise ValueError("q must be [B,Hq,D] and caches [B,Smax,Hkv,D]")
+    B, Hq, D = q.shape
+    Bk, Smax, Hkv, Dk = kcache.shape
+    if Bk != B or Dk != D or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("shape mismatch between q and the caches")
+    if q.dtype != kcache.dtype or q.dtype != vcache.dtype:
+        raise TypeError("q and the caches must share a dtype")
+    code = _dtype_code(q)
+    if cache_seqlens.dtype != torch.int32 or tuple(cache_seqlens.shape) != (B,):
+        raise ValueError("cache_seqlens must be int32 [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    need = gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, Smax)
+    if workspace is None and need > 0:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
+    dev = _check_cuda(q, kcache, vcache, cache_seqlens, out, workspace)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().gqa_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_seqlens), _ptr(out),
+                                   B, Hq, Hkv, D, float(scale), int(num_splits), Smax, code,
+                                   _ptr(workspace), wbytes, _stream(dev, stream))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_decode")
+    return out
+
+
+def gqa_device_status(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    torch = _torch()
+    st = stream if stream is not None else torch.cuda.current_stream()
+    return int(load_library().gqa_device_status(ctypes.c_void_p(st.cuda_stream)))

@@ -1,0 +1,368 @@
+// gqa_api.cu -- the C ABI of libgqa (declared in include/gqa.h): argument
+// validation, TMA tensor-map encoding, split planning and kernel launches.
+// One translation unit holds every kernel so that they share the device
+// error word.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <algorithm>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "gqa.h"
+#include "common.cuh"
+#include "prefill_sm103.cuh"
+#include "decode_sm103.cuh"
+#include "fp32_check.cuh"
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 128;
+
+// ----------------------------------------------------------------- helpers
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int num_sms(int dev) {
+  static int cache[kMaxDevices] = {0};
+  if (dev < 0 || dev >= kMaxDevices) return 148;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return 0;
+  return d;
+}
+
+unsigned long long wait_timeout_ns() {
+  static unsigned long long v = [] {
+    const char* e = std::getenv("GQA_WAIT_TIMEOUT_NS");
+    unsigned long long t = e ? std::strtoull(e, nullptr, 10) : 0ull;
+    return t > 0 ? t : 2000000000ull;   // 2 s
+  }();
+  return v;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D bf16 tensor map over a row-major [d3][d2][d1][d0] array, 128-byte
+// swizzle, out-of-bounds elements read as zero.
+bool encode_4d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t d3,
+                    uint32_t b0, uint32_t b1, uint32_t b2, uint32_t b3) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {d0, d1, d2, d3};
+  const cuuint64_t strides[3] = {d0 * 2, d0 * d1 * 2, d0 * d1 * d2 * 2};
+  const cuuint32_t box[4] = {b0, b1, b2, b3};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Sets the dynamic shared-memory size once per device and checks that the
+// compiled register count is the one the setmaxnreg split was sized for: the
+// softmax warpgroups' setmaxnreg.inc can only complete if the block was
+// launched with kLaunchRegs registers per thread.
+template <int D>
+bool prefill_smem_attr_set(int dev) {
+  namespace pf = gqa::prefill;
+  static bool done[kMaxDevices] = {false};
+  if (dev >= 0 && dev < kMaxDevices && done[dev]) return true;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, pf::prefill_kernel<D>) != cudaSuccess) return false;
+  static_assert(2 * 128 * pf::kSoftmaxRegs + 128 * pf::kOtherRegs <= pf::kThreads * pf::kLaunchRegs,
+                "register split exceeds the launch budget");
+  if (fa.numRegs != pf::kLaunchRegs) return false;
+  if (cudaFuncSetAttribute(pf::prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(pf::Layout<D>::kSmemAlloc)) != cudaSuccess)
+    return false;
+  if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
+  return true;
+}
+
+template <int D>
+int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
+                        int Sq, int Sk, float scale, int causal, const int* seqlens_k, cudaStream_t stream) {
+  namespace pf = gqa::prefill;
+  const int G = Hq / Hkv;
+  const int Mq = pf::kBM / G;
+  const long long n_qblk = (Sq + pf::kNQT * Mq - 1) / (pf::kNQT * Mq);
+  const long long grid = n_qblk * B * Hkv;
+  if (grid <= 0 || grid > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  CUtensorMap tmQ, tmK, tmV;
+  if (!encode_4d_bf16(&tmQ, q, D, Hq, Sq, B, 64, G, Mq, 1) || !encode_4d_bf16(&tmK, k, D, Hkv, Sk, B, 64, 1, 128, 1) ||
+      !encode_4d_bf16(&tmV, v, D, Hkv, Sk, B, 64, 1, 128, 1))
+    return GQA_ERR_CUDA;
+  if (!prefill_smem_attr_set<D>(current_device())) return GQA_ERR_CUDA;
+  pf::Params p;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.lse = lse;
+  p.seqlens = seqlens_k;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.Mq = Mq;
+  p.n_qblk = int(n_qblk);
+  p.causal = causal ? 1 : 0;
+  p.scale_log2 = scale * kLog2e;
+  p.timeout_ns = wait_timeout_ns();
+  pf::prefill_kernel<D><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(tmQ, tmK, tmV, p);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+int launch_f32(const gqa::f32::Params& p, cudaStream_t stream) {
+  const long long rows = (long long)p.B * p.Hq * p.Sq;
+  const long long gx = (rows + gqa::f32::kWarps - 1) / gqa::f32::kWarps;
+  if (gx > 0x7fffffffLL || p.nsplit > 65535) return GQA_ERR_UNSUPPORTED;
+  gqa::f32::attention_kernel<<<dim3(unsigned(gx), unsigned(p.nsplit)), gqa::f32::kWarps * 32, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
+
+struct SplitPlan {
+  int n;          // number of splits actually launched
+  int len;        // keys per split (multiple of 16)
+};
+
+// n requested (<= 0: automatic) -> split length rounded up to 16 keys; the
+// launched count is ceil(Smax / len) so that no split is empty for a full cache.
+SplitPlan plan_splits(int B, int Hkv, int Smax, int num_splits) {
+  int n = num_splits;
+  if (n <= 0) {
+    // automatic: about 1024 keys per split, and enough CTAs for several waves
+    const int sms = num_sms(current_device());
+    n = (Smax + 1023) / 1024;
+    const long long want = 4LL * sms;
+    while ((long long)n * B * Hkv < want && n < kMaxSplits && (Smax + n) / (n + 1) >= 256) ++n;
+  }
+  n = std::max(1, std::min(n, kMaxSplits));
+  const int blocks = (Smax + 15) / 16;
+  n = std::min(n, blocks);
+  int len = (Smax + n - 1) / n;
+  len = (len + 15) / 16 * 16;
+  SplitPlan sp;
+  sp.len = len;
+  sp.n = (Smax + len - 1) / len;
+  return sp;
+}
+
+size_t workspace_for(int B, int Hq, int D, int n) {
+  if (n <= 1) return 0;
+  const size_t o = size_t(B) * Hq * n * D * sizeof(float);
+  const size_t l = size_t(B) * Hq * n * sizeof(float);
+  return ((o + 255) / 256) * 256 + l;
+}
+
+}  // namespace
+
+// ====================================================================== ABI
+extern "C" {
+
+const char* gqa_status_string(int status) {
+  switch (status) {
+    case GQA_OK: return "GQA_OK";
+    case GQA_ERR_INVALID_ARG: return "GQA_ERR_INVALID_ARG";
+    case GQA_ERR_UNSUPPORTED: return "GQA_ERR_UNSUPPORTED";
+    case GQA_ERR_CUDA: return "GQA_ERR_CUDA";
+    case GQA_ERR_DEVICE_TIMEOUT: return "GQA_ERR_DEVICE_TIMEOUT";
+    case GQA_ERR_DEVICE_BOUNDS: return "GQA_ERR_DEVICE_BOUNDS";
+    default: return "GQA_ERR_UNKNOWN";
+  }
+}
+
+int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv, int Sq,
+            int Sk, int D, float scale, int causal, const int* seqlens_k, int dtype, void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return GQA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
+  if ((lse && !aligned(lse, 4)) || (seqlens_k && !aligned(seqlens_k, 4))) return GQA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == GQA_DTYPE_BF16) {
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return GQA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+    if (Hq / Hkv > gqa::prefill::kBM) return GQA_ERR_UNSUPPORTED;
+    if ((long long)Hq * D * Sq * B > (1LL << 40)) return GQA_ERR_UNSUPPORTED;
+    return D == 64 ? launch_prefill_bf16<64>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k, st)
+                   : launch_prefill_bf16<128>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k, st);
+  }
+  if (dtype == GQA_DTYPE_FP32) {
+    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4)) return GQA_ERR_INVALID_ARG;
+    if (D > gqa::f32::kMaxD) return GQA_ERR_UNSUPPORTED;
+    gqa::f32::Params p{};
+    p.q = static_cast<const float*>(q);
+    p.k = static_cast<const float*>(k);
+    p.v = static_cast<const float*>(v);
+    p.out = static_cast<float*>(out);
+    p.lse = lse;
+    p.seqlens = seqlens_k;
+    p.q_sb = (long long)Sq * Hq * D;
+    p.q_ss = (long long)Hq * D;
+    p.q_sh = D;
+    p.k_sb = (long long)Sk * Hkv * D;
+    p.k_ss = (long long)Hkv * D;
+    p.k_sh = D;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.D = D;
+    p.causal = causal;
+    p.scale = scale;
+    p.nsplit = 1;
+    p.split_len = Sk;
+    p.len_cap = Sk;
+    return launch_f32(p, st);
+  }
+  return GQA_ERR_INVALID_ARG;
+}
+
+int gqa_decode_num_splits(int B, int Hkv, int max_seqlen_k, int num_splits) {
+  if (B <= 0 || Hkv <= 0 || max_seqlen_k <= 0) return -GQA_ERR_INVALID_ARG;
+  if (num_splits > kMaxSplits) return -GQA_ERR_INVALID_ARG;
+  return plan_splits(B, Hkv, max_seqlen_k, num_splits).n;
+}
+
+size_t gqa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits, int max_seqlen_k) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_seqlen_k <= 0 || num_splits > kMaxSplits) return 0;
+  return workspace_for(B, Hq, D, plan_splits(B, Hkv, max_seqlen_k, num_splits).n);
+}
+
+int gqa_decode(const void* q, const void* kcache, const void* vcache, const int* cache_seqlens, void* out, int B,
+               int Hq, int Hkv, int D, float scale, int num_splits, int max_seqlen_k, int dtype, void* workspace,
+               size_t workspace_bytes, void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_seqlen_k <= 0) return GQA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || num_splits > kMaxSplits) return GQA_ERR_INVALID_ARG;
+  if (!q || !kcache || !vcache || !cache_seqlens || !out) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !aligned(cache_seqlens, 4)) return GQA_ERR_INVALID_ARG;
+  const SplitPlan sp = plan_splits(B, Hkv, max_seqlen_k, num_splits);
+  const size_t need = workspace_for(B, Hq, D, sp.n);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16))) return GQA_ERR_INVALID_ARG;
+  float* part_o = static_cast<float*>(workspace);
+  float* part_lse = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                    ((size_t(B) * Hq * sp.n * D * sizeof(float) + 255) / 256) * 256)
+                         : nullptr;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int G = Hq / Hkv;
+  if (dtype == GQA_DTYPE_BF16) {
+    if (!aligned(q, 16) || !aligned(kcache, 16) || !aligned(vcache, 16) || !aligned(out, 16))
+      return GQA_ERR_INVALID_ARG;
+    if ((D != 64 && D != 128) || G > 8) return GQA_ERR_UNSUPPORTED;
+    if (B > 65535 || Hkv > 65535) return GQA_ERR_UNSUPPORTED;
+    gqa::decode::Params p;
+    p.q = static_cast<const __nv_bfloat16*>(q);
+    p.kc = static_cast<const __nv_bfloat16*>(kcache);
+    p.vc = static_cast<const __nv_bfloat16*>(vcache);
+    p.seqlens = cache_seqlens;
+    p.out = static_cast<__nv_bfloat16*>(out);
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = G;
+    p.Smax = max_seqlen_k;
+    p.nsplit = sp.n;
+    p.split_len = sp.len;
+    p.scale_log2 = scale * kLog2e;
+    const dim3 grid(sp.n, Hkv, B);
+    if (D == 64)
+      gqa::decode::decode_split_kernel<64><<<grid, gqa::decode::kThreads, 0, st>>>(p);
+    else
+      gqa::decode::decode_split_kernel<128><<<grid, gqa::decode::kThreads, 0, st>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    if (sp.n > 1) {
+      const int rows = B * Hq;
+      gqa::decode::combine_kernel<__nv_bfloat16><<<(rows + 3) / 4, 128, 0, st>>>(
+          part_o, part_lse, cache_seqlens, static_cast<__nv_bfloat16*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
+      if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+  }
+  if (dtype == GQA_DTYPE_FP32) {
+    if (!aligned(q, 4) || !aligned(kcache, 4) || !aligned(vcache, 4) || !aligned(out, 4))
+      return GQA_ERR_INVALID_ARG;
+    if (D > gqa::f32::kMaxD) return GQA_ERR_UNSUPPORTED;
+    gqa::f32::Params p{};
+    p.q = static_cast<const float*>(q);
+    p.k = static_cast<const float*>(kcache);
+    p.v = static_cast<const float*>(vcache);
+    p.out = static_cast<float*>(out);
+    p.lse = nullptr;
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    p.seqlens = cache_seqlens;
+    p.q_sb = (long long)Hq * D;
+    p.q_ss = 0;
+    p.q_sh = D;
+    p.k_sb = (long long)max_seqlen_k * Hkv * D;
+    p.k_ss = (long long)Hkv * D;
+    p.k_sh = D;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = G;
+    p.Sq = 1;
+    p.Sk = max_seqlen_k;
+    p.D = D;
+    p.causal = 0;
+    p.scale = scale;
+    p.nsplit = sp.n;
+    p.split_len = sp.len;
+    p.len_cap = max_seqlen_k;
+    const int rc = launch_f32(p, st);
+    if (rc != GQA_OK) return rc;
+    if (sp.n > 1) {
+      const int rows = B * Hq;
+      gqa::decode::combine_kernel<float><<<(rows + 3) / 4, 128, 0, st>>>(
+          part_o, part_lse, cache_seqlens, static_cast<float*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
+      if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+    }
+    return GQA_OK;
+  }
+  return GQA_ERR_INVALID_ARG;
+}
+
+int gqa_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return GQA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, gqa::g_error_word, sizeof(v)) != cudaSuccess) return GQA_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(gqa::g_error_word, &zero, sizeof(zero)) != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  return int(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,437 @@
+// prefill_sm103.cuh -- bf16 grouped-query attention forward (prefill) for
+// sm_103a: TMA + tcgen05.mma with TMEM accumulators, warp-specialised.
+//
+// Method (sources cited by page title and section):
+//  * "3个GQA核心优化技巧" (blog.gitcode.com), "GQA的分组共享机制" and
+//    "Flash-Attention的稀疏分组优化": the G = Hq/Hkv query heads of a group
+//    read one K/V head (kvh = h / G), and a K/V block brought on chip once is
+//    reused by every query head of the group.  Here the G heads of a group
+//    are packed into the M dimension of one 128-row MMA tile (row = token *
+//    G + head-in-group), so each K/V tile is loaded once per CTA and feeds
+//    all of them.
+//  * "FlashAttention Serisi" (webturing.pages.dev), "Ana fikir": scores are
+//    consumed tile by tile with a running maximum and running sum (online
+//    softmax) and never written to global memory; "V3 ve donanım uyumu":
+//    producer warps move data while consumer warps compute.
+//
+// CTA work unit: batch b, K/V head kvh, and 2 consecutive Q tiles of Mq =
+// floor(128/G) tokens x G heads each.  Warp roles (384 threads):
+//   warps 0-3  softmax for Q tile 0 (thread = one row = one TMEM lane)
+//   warps 4-7  softmax for Q tile 1
+//   warp  8    TMA producer: Q tiles once, then a K ring and a V ring
+//   warp  9    MMA issuer: S_t = Q_t K^T into TMEM, O_t += P_t V with P_t
+//              read from TMEM (P overwrites S_t as packed bf16)
+//   warps 10-11 idle (they complete the third warpgroup, which hands its
+//              registers to the softmax warpgroups with setmaxnreg)
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+// The two softmax warpgroups ping-pong: while one computes exponentials the
+// tensor core runs the other's PV and next QK^T.
+//
+// Softmax details: t = s * scale * log2(e); the running max m is only moved
+// when a tile's max exceeds it by more than 8 (log2 units); otherwise the
+// stale m is kept, probabilities are bounded by 2^8 and the final division
+// by l = sum p is exact for any reference m.  Masked keys (j >= L_b, or
+// j > i + Sk - Sq when causal) get p = 0 exactly.
+#pragma once
+
+#include "common.cuh"
+
+namespace gqa {
+namespace prefill {
+
+constexpr int kBM = 128;       // rows per Q tile (= TMEM lanes)
+constexpr int kBN = 128;       // keys per K/V tile
+constexpr int kNQT = 2;        // Q tiles per CTA
+constexpr int kWarpTMA = 8;
+constexpr int kWarpMMA = 9;
+constexpr int kThreads = 384;
+constexpr int kSoftmaxRegs = 216;   // 2 x 128 x 216 + 128 x 72 = 384 x 168 registers at launch
+constexpr int kLaunchRegs = 168;
+constexpr int kOtherRegs = 72;
+constexpr float kRescaleThreshold = 8.0f;
+
+template <int D>
+struct Layout {
+  static constexpr int kHalves = D / 64;                    // 64-column (128-byte) halves of a row
+  static constexpr int kStages = (D == 64) ? 3 : 2;         // depth of the K ring and of the V ring
+  static constexpr uint32_t kHalfBytes = 128u * 128u;       // 128 rows x 128 bytes
+  static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffK = kOffQ + kNQT * kTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_done[2], drain
+  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kNQT + 1;
+  static constexpr uint32_t kOffTmemSlot = kOffBar + 8u * kNumBars;
+  static constexpr uint32_t kOffAbort = kOffTmemSlot + 8u;
+  static constexpr uint32_t kBytes = kOffAbort + 8u;
+  static constexpr uint32_t kSmemAlloc = kBytes + 1024u;    // slack to align the base to 1024 B
+  // V is the MN-major B operand: 8-key groups 1024 B apart (SBO); the second
+  // 64-wide head-dim half (D = 128) is kHalfBytes further (LBO).  With D = 64
+  // the LBO is never used and is set to 1024 so the descriptor stays inside
+  // the stage whichever way the two offsets are read.
+  static constexpr uint32_t kVLbo = (D == 64) ? 1024u : kHalfBytes;
+  static constexpr uint32_t kTmCols = 512;
+  static constexpr uint32_t kTmS0 = 0, kTmS1 = 128;
+  static constexpr uint32_t kTmO0 = 256, kTmO1 = 256 + D;
+};
+
+struct Params {
+  __nv_bfloat16* out;     // [B, Sq, Hq, D]
+  float* lse;             // [B, Hq, Sq] or nullptr
+  const int* seqlens;     // [B] or nullptr
+  int B, Hq, Hkv, G, Sq, Sk;
+  int Mq;                 // tokens per Q tile (G * Mq <= 128)
+  int n_qblk;             // ceil(Sq / (kNQT * Mq))
+  int causal;
+  float scale_log2;       // scale * log2(e)
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using L = Layout<D>;
+  constexpr int S = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw_addr);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work unit: causal launches take the longest (last) q blocks first
+  const int bh_count = p.B * p.Hkv;
+  int qblk = blockIdx.x / bh_count;
+  if (p.causal) qblk = p.n_qblk - 1 - qblk;
+  const int bh = blockIdx.x % bh_count;
+  const int b = bh / p.Hkv;
+  const int kvh = bh % p.Hkv;
+  const int q0 = qblk * kNQT * p.Mq;
+  const int rows_per_tile = p.G * p.Mq;
+
+  int Lb = p.seqlens ? p.seqlens[b] : p.Sk;
+  const bool bad_len = (Lb < 0 || Lb > p.Sk);
+  if (bad_len) Lb = 0;
+  const int q_last = min(q0 + kNQT * p.Mq, p.Sq) - 1;
+  int kmax = Lb;
+  if (p.causal) kmax = min(kmax, q_last + p.Sk - p.Sq + 1);
+  const int n_tiles = kmax > 0 ? (kmax + kBN - 1) / kBN : 0;
+
+  auto bar = [&](int i) -> uint32_t { return base + L::kOffBar + 8u * uint32_t(i); };
+  const uint32_t q_full = bar(0);
+  auto k_full = [&](int s) { return bar(1 + s); };
+  auto k_empty = [&](int s) { return bar(1 + S + s); };
+  auto v_full = [&](int s) { return bar(1 + 2 * S + s); };
+  auto v_empty = [&](int s) { return bar(1 + 3 * S + s); };
+  auto s_full = [&](int t) { return bar(1 + 4 * S + t); };
+  auto p_full = [&](int t) { return bar(1 + 4 * S + kNQT + t); };
+  auto o_done = [&](int t) { return bar(1 + 4 * S + 2 * kNQT + t); };
+  const uint32_t drain = bar(1 + 4 * S + 3 * kNQT);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffTmemSlot);
+  const uint64_t to = p.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(k_full(s), 1);
+      mbar_init(k_empty(s), 1);
+      mbar_init(v_full(s), 1);
+      mbar_init(v_empty(s), 1);
+    }
+    for (int t = 0; t < kNQT; ++t) {
+      mbar_init(s_full(t), 1);
+      mbar_init(p_full(t), 128);
+      mbar_init(o_done(t), 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    if (bad_len) raise_error(kErrBounds);
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == kWarpMMA) {
+    tmem_alloc(smem_u32(tmem_slot), L::kTmCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpTMA && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp >= 8) {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+  if (warp == kWarpTMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n_tiles > 0) {
+      int issued = 0;
+      bool ok = true;
+      const uint32_t q_bytes = uint32_t(kNQT * L::kHalves * 64 * 2 * rows_per_tile);
+      mbar_arrive_expect_tx(q_full, q_bytes);
+      for (int t = 0; t < kNQT; ++t)
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_4d(base + L::kOffQ + t * L::kTileBytes + h * L::kHalfBytes, &tmQ, q_full, h * 64,
+                      kvh * p.G, q0 + t * p.Mq, b);
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int s = j % S;
+        const uint32_t ph = (j / S) & 1;
+        ok = mbar_wait(k_empty(s), ph ^ 1, abort_flag, to);
+        if (!ok) break;
+        mbar_arrive_expect_tx(k_full(s), L::kTileBytes);
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_4d(base + L::kOffK + s * L::kTileBytes + h * L::kHalfBytes, &tmK, k_full(s), h * 64,
+                      kvh, j * kBN, b);
+        ok = mbar_wait(v_empty(s), ph ^ 1, abort_flag, to);
+        if (!ok) break;
+        mbar_arrive_expect_tx(v_full(s), L::kTileBytes);
+        for (int h = 0; h < L::kHalves; ++h)
+          tma_load_4d(base + L::kOffV + s * L::kTileBytes + h * L::kHalfBytes, &tmV, v_full(s), h * 64,
+                      kvh, j * kBN, b);
+        issued = j + 1;
+      }
+      if (!ok) {
+        // aborted: let the copies already in flight land before the CTA exits
+        volatile int no_abort = 0;
+        for (int j = max(0, issued - S); j < issued; ++j) {
+          mbar_wait(k_full(j % S), (j / S) & 1, &no_abort, 200000000ull);
+          mbar_wait(v_full(j % S), (j / S) & 1, &no_abort, 200000000ull);
+        }
+      }
+    }
+  } else if (warp == kWarpMMA) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && n_tiles > 0) {
+      const uint32_t idesc_s = make_idesc_bf16(128, kBN, 0, 0);   // Q, K both K-major
+      const uint32_t idesc_o = make_idesc_bf16(128, D, 0, 1);     // P (TMEM), V MN-major
+      auto issue_s = [&](int t, int s) {
+        const uint32_t qa = base + L::kOffQ + t * L::kTileBytes;
+        const uint32_t ka = base + L::kOffK + s * L::kTileBytes;
+        const uint32_t dst = tmem + (t ? L::kTmS1 : L::kTmS0);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = uint32_t(ks / 4) * L::kHalfBytes + uint32_t(ks % 4) * 32u;
+          umma_ss(dst, make_sdesc_sw128(qa + off, 16, 1024), make_sdesc_sw128(ka + off, 16, 1024),
+                  idesc_s, ks > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_pv = [&](int t, int s, bool acc) {
+        const uint32_t va = base + L::kOffV + s * L::kTileBytes;
+        const uint32_t dst = tmem + (t ? L::kTmO1 : L::kTmO0);
+        const uint32_t pa = tmem + (t ? L::kTmS1 : L::kTmS0);
+#pragma unroll
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          umma_ts(dst, pa + uint32_t(ks) * 8u, make_sdesc_sw128(va + uint32_t(ks) * 2048u, L::kVLbo, 1024),
+                  idesc_o, (acc || ks > 0) ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, to) && mbar_wait(k_full(0), 0, abort_flag, to);
+      if (ok) {
+        tc_fence_after();
+        for (int t = 0; t < kNQT; ++t) {
+          issue_s(t, 0);
+          umma_commit(s_full(t));
+        }
+        umma_commit(k_empty(0));
+      }
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int s = j % S;
+        const uint32_t ph = (j / S) & 1;
+        const int nj = j + 1;
+        const bool has_next = nj < n_tiles;
+        const int ns = nj % S;
+        const uint32_t nph = (nj / S) & 1;
+        ok = mbar_wait(v_full(s), ph, abort_flag, to);
+        if (ok && has_next) ok = mbar_wait(k_full(ns), nph, abort_flag, to);
+        for (int t = 0; ok && t < kNQT; ++t) {
+          ok = mbar_wait(p_full(t), j & 1, abort_flag, to);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(t, s, j > 0);
+          umma_commit(o_done(t));
+          if (has_next) {
+            issue_s(t, ns);
+            umma_commit(s_full(t));
+          }
+        }
+        if (!ok) break;
+        umma_commit(v_empty(s));
+        if (has_next) umma_commit(k_empty(ns));
+      }
+      if (!ok) {
+        // aborted: wait for the tensor core to finish what was issued
+        volatile int no_abort = 0;
+        umma_commit(drain);
+        mbar_wait(drain, 0, &no_abort, 200000000ull);
+      }
+    }
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
+    // ------------------------------------------------------------- softmax
+    const int t = warp >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
+    const uint32_t lane_base = uint32_t(wq * 32) << 16;
+    const uint32_t tS = tmem + lane_base + (t ? L::kTmS1 : L::kTmS0);
+    const uint32_t tO = tmem + lane_base + (t ? L::kTmO1 : L::kTmO0);
+    const int token = q0 + t * p.Mq + r / p.G;
+    const int g = r % p.G;
+    const bool row_ok = (r < rows_per_tile) && (token < p.Sq);
+    int limit = 0;
+    if (row_ok) {
+      limit = Lb;
+      if (p.causal) limit = min(limit, token + p.Sk - p.Sq + 1);
+      limit = max(limit, 0);
+    }
+    const float c = p.scale_log2;
+    float m = -INFINITY;
+    float l = 0.f;
+    bool aborted = false;
+
+    for (int j = 0; j < n_tiles; ++j) {
+      bool ok = mbar_wait(s_full(t), j & 1, abort_flag, to);
+      if (ok && j > 0) ok = mbar_wait(o_done(t), (j - 1) & 1, abort_flag, to);
+      if (!__all_sync(0xffffffffu, ok)) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sv[kBN];
+      tmem_ld_32x32b_x32(tS + 0, sv + 0);
+      tmem_ld_32x32b_x32(tS + 32, sv + 32);
+      tmem_ld_32x32b_x32(tS + 64, sv + 64);
+      tmem_ld_32x32b_x32(tS + 96, sv + 96);
+      tmem_ld_wait_x128(sv);
+
+      const int lim = limit - j * kBN;
+      const bool full_tile = lim >= kBN;
+      float mt;
+      if (full_tile) {
+        // every key of the tile is admissible for this row
+        float e0 = __uint_as_float(sv[0]), e1 = e0;
+        if (c >= 0.f) {
+#pragma unroll
+          for (int i = 1; i < kBN; i += 2) {
+            e0 = fmaxf(e0, __uint_as_float(sv[i]));
+            if (i + 1 < kBN) e1 = fmaxf(e1, __uint_as_float(sv[i + 1]));
+          }
+        } else {
+#pragma unroll
+          for (int i = 1; i < kBN; i += 2) {
+            e0 = fminf(e0, __uint_as_float(sv[i]));
+            if (i + 1 < kBN) e1 = fminf(e1, __uint_as_float(sv[i + 1]));
+          }
+        }
+        mt = (c >= 0.f ? fmaxf(e0, e1) : fminf(e0, e1)) * c;
+      } else {
+        // edge tile: scale, mask and keep the scaled values
+        mt = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) {
+          const float f = (i < lim) ? __uint_as_float(sv[i]) * c : -INFINITY;
+          sv[i] = __float_as_uint(f);
+          mt = fmaxf(mt, f);
+        }
+      }
+      const float m_new = fmaxf(m, mt);
+      const bool need = m_new > m + kRescaleThreshold;
+      float alpha = 1.f;
+      if (need) {
+        alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+        l *= alpha;
+        m = m_new;
+      }
+      if (__any_sync(0xffffffffu, need && j > 0)) {
+        // move O_t to the new reference maximum (the previous PV has completed:
+        // this tile's S was committed after it)
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(tO + cc, o);
+          tmem_ld_wait_x32(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st_32x32b_x32(tO + cc, o);
+        }
+      }
+      const float mref = (m == -INFINITY) ? 0.f : m;
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int k0 = q * 32 + 2 * i;
+          float p0, p1;
+          if (full_tile) {
+            p0 = ex2_approx(fmaf(__uint_as_float(sv[k0]), c, -mref));
+            p1 = ex2_approx(fmaf(__uint_as_float(sv[k0 + 1]), c, -mref));
+          } else {
+            p0 = ex2_approx(__uint_as_float(sv[k0]) - mref);
+            p1 = ex2_approx(__uint_as_float(sv[k0 + 1]) - mref);
+          }
+          ls0 += p0;
+          ls1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
+      }
+      l += ls0 + ls1;
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(p_full(t));
+    }
+
+    // ------------------------------------------------------------ epilogue
+    bool have_o = (n_tiles > 0) && !aborted;
+    if (have_o) {
+      const bool ok = mbar_wait(o_done(t), (n_tiles - 1) & 1, abort_flag, to);
+      have_o = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    const float inv_l = (l > 0.f && have_o) ? 1.f / l : 0.f;
+    __nv_bfloat16* orow = p.out + ((size_t(b) * p.Sq + token) * p.Hq + (size_t(kvh) * p.G + g)) * D;
+#pragma unroll
+    for (int cc = 0; cc < D; cc += 32) {
+      uint32_t o[32];
+      if (have_o) {
+        tmem_ld_32x32b_x32(tO + cc, o);
+        tmem_ld_wait_x32(o);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[i] = 0u;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4)
+          dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+      }
+    }
+    if (row_ok && p.lse) {
+      const float lse = (l > 0.f && have_o) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+      p.lse[(size_t(b) * p.Hq + size_t(kvh) * p.G + g) * p.Sq + token] = lse;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmCols);
+  }
+}
+
+}  // namespace prefill
+}  // namespace gqa

@@ -1,0 +1,166 @@
+/*
+ * gqa.h -- C ABI of libgqa, a grouped-query attention (GQA) forward library
+ * for NVIDIA B300 (sm_103a).
+ *
+ * What it computes (sources cited by page title and section):
+ *   [GQA-BERT]  "3个GQA核心优化技巧：解决BERT模型内存效率与吞吐量瓶颈"
+ *               (blog.gitcode.com): "GQA的分组共享机制" -- Hq query heads are
+ *               split into groups that share one K/V head, Hq % Hkv == 0,
+ *               group size G = Hq / Hkv; "Flash-Attention的稀疏分组优化" --
+ *               query head h reads K/V head h / G, and a K/V block staged in
+ *               shared memory is reused by every query head of its group;
+ *               "阶段二" -- softmax scale 1/sqrt(d_head), causal off for
+ *               BERT, num_splits for split computation, seqlen_k hint.
+ *   [GQA-PAPER] "GQA: Training Generalized Multi-Query Transformer Models
+ *               from Multi-Head Checkpoints" (azimuth.plus/paper/gqa):
+ *               "Idea 2" (GQA-H = MHA, GQA-1 = MQA, contiguous groups),
+ *               "Problem"/"Bottleneck" (a decode step reads the whole KV
+ *               cache; it is bandwidth bound), KV_cache_size equation.
+ *   [LOWRANK]   aifullclass.xyz BERT attention article, code example:
+ *               softmax(Q K^T * scale, masked keys excluded) V.
+ *   [FA-SERIES] "FlashAttention Serisi: Bellek G/Ç Tıkanıklığının Çözümü"
+ *               (webturing.pages.dev): "Ana fikir" (tiled online softmax,
+ *               scores never written to slow memory, identical result),
+ *               "V3 ve donanım uyumu" (warp-specialised producer/consumer).
+ *
+ *   For batch b, query head h (K/V head kvh = h / G), query row i:
+ *     L_b = seqlens_k ? seqlens_k[b] : Sk          (right-padded keys)
+ *     J   = { j < L_b  and  (!causal or j <= i + Sk - Sq) }
+ *     out[b,i,h,:] = sum_{j in J} softmax_j(scale * q.k_j) v_j
+ *     lse[b,h,i]   = ln sum_{j in J} exp(scale * q.k_j)
+ *   An empty J gives out = 0 and lse = -inf.  Keys outside J get exactly
+ *   zero weight (the page's -1e9 fill read as "never attended").
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the
+ *     library keeps no reference after the call returns and allocates no
+ *     device memory per call.
+ *   - Layouts are row-major and contiguous (BSHD, head dimension last):
+ *       q, out [B, Sq, Hq, D];  k, v [B, Sk, Hkv, D];  lse [B, Hq, Sq] fp32
+ *       decode: q, out [B, Hq, D];  kcache, vcache [B, Smax, Hkv, D]
+ *   - dtype: GQA_DTYPE_BF16 (q/k/v/out bfloat16, fp32 accumulation,
+ *     tcgen05 tensor cores) or GQA_DTYPE_FP32 (q/k/v/out float32, exact
+ *     fp32 SIMT check path).  lse is always float32.
+ *   - stream is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work: they never synchronise, so errors found on the device
+ *     (a key length out of range, a pipeline wait that timed out) are
+ *     reported later by gqa_device_status().
+ *   - Return value: a gqa_status code.  On any non-OK return nothing has
+ *     been enqueued.
+ */
+#ifndef GQA_H_
+#define GQA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    GQA_OK = 0,
+    GQA_ERR_INVALID_ARG = 1,     /* bad size, pointer, alignment, Hq % Hkv != 0, ... */
+    GQA_ERR_UNSUPPORTED = 2,     /* valid but not implemented (e.g. bf16 with D not 64/128) */
+    GQA_ERR_CUDA = 3,            /* a CUDA runtime/driver call failed */
+    GQA_ERR_DEVICE_TIMEOUT = 4,  /* a device-side pipeline wait gave up (reported by gqa_device_status) */
+    GQA_ERR_DEVICE_BOUNDS = 5    /* a device-side length check failed (reported by gqa_device_status) */
+} gqa_status;
+
+typedef enum {
+    GQA_DTYPE_BF16 = 0,
+    GQA_DTYPE_FP32 = 1
+} gqa_dtype;
+
+/*
+ * gqa_fwd -- prefill / encoder attention, non-causal (BERT) or causal.
+ * [GQA-BERT] "GQA的分组共享机制", "Flash-Attention的稀疏分组优化", "阶段二";
+ * [LOWRANK] code example; [FA-SERIES] "Ana fikir".
+ *
+ *   q         [B, Sq, Hq, D]   device, read
+ *   k, v      [B, Sk, Hkv, D]  device, read
+ *   out       [B, Sq, Hq, D]   device, written (same dtype as q)
+ *   lse       [B, Hq, Sq] fp32 device, written; may be NULL (not written)
+ *   B, Hq, Hkv, Sq, Sk, D      sizes, all >= 1; Hq % Hkv == 0 ([GQA-BERT])
+ *   scale     finite softmax scale (the pages use 1/sqrt(D))
+ *   causal    0: every query sees keys [0, L_b); 1: query row i also
+ *             requires j <= i + Sk - Sq (bottom-right aligned)
+ *   seqlens_k int32 [B] device, key lengths L_b in [0, Sk]; NULL = all Sk.
+ *             Values outside [0, Sk] make the affected batch entry write
+ *             zeros and raise GQA_ERR_DEVICE_BOUNDS in gqa_device_status().
+ *   dtype     gqa_dtype
+ *   stream    cudaStream_t
+ * bf16: D must be 64 or 128 and G = Hq/Hkv <= 128; q/k/v/out 16-byte aligned.
+ * fp32: 1 <= D <= 256; 4-byte aligned.
+ * Returns GQA_OK, GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED or GQA_ERR_CUDA.
+ */
+int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
+            int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+            const int* seqlens_k, int dtype, void* stream);
+
+/*
+ * gqa_decode_num_splits -- the number of KV-length splits gqa_decode will use.
+ * num_splits > 0 is returned unchanged (clamped to 128 and to the number of
+ * 16-key blocks of max_seqlen_k); num_splits <= 0 asks for the automatic
+ * choice, which sizes the grid to fill the GPU of the current device.
+ * Split s of every sequence covers keys [s*Ls, (s+1)*Ls) with
+ * Ls = ceil(max_seqlen_k / n) rounded up to 16 ([GQA-BERT] "阶段二":
+ * num_splits cuts the key range into pieces computed independently).
+ * Returns n >= 1, or a negative gqa_status on bad arguments.
+ */
+int gqa_decode_num_splits(int B, int Hkv, int max_seqlen_k, int num_splits);
+
+/*
+ * gqa_decode_workspace_bytes -- device scratch gqa_decode needs for the
+ * split partials: fp32 O_s [B, Hq, n, D] plus fp32 lse_s [B, Hq, n], where
+ * n = gqa_decode_num_splits(B, Hkv, max_seqlen_k, num_splits).  Returns 0
+ * when n == 1 (no combine step) and 0 for invalid arguments.
+ */
+size_t gqa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits,
+                                  int max_seqlen_k);
+
+/*
+ * gqa_decode -- one generated token per sequence attending to its KV cache.
+ * [GQA-PAPER] "Problem"/"Bottleneck" (every step reads the whole cache);
+ * [GQA-BERT] "阶段二" (num_splits); [FA-SERIES] "Ana fikir" (split partial
+ * softmax results merge exactly through their log-sum-exp).
+ *
+ *   q              [B, Hq, D]          device, read
+ *   kcache, vcache [B, Smax, Hkv, D]   device, read; Smax = max_seqlen_k
+ *   cache_seqlens  int32 [B]           device; L_b in [0, Smax].  Out-of-range
+ *                  values write zeros for that entry and raise
+ *                  GQA_ERR_DEVICE_BOUNDS in gqa_device_status().
+ *   out            [B, Hq, D]          device, written
+ *   B, Hq, Hkv, D  sizes; Hq % Hkv == 0
+ *   scale          finite softmax scale
+ *   num_splits     <= 0 automatic, else 1..128 (see gqa_decode_num_splits)
+ *   max_seqlen_k   Smax, the cache capacity (row stride of the caches)
+ *   dtype          gqa_dtype
+ *   workspace      device scratch of at least gqa_decode_workspace_bytes()
+ *                  bytes, 16-byte aligned; may be NULL when that is 0.
+ *                  Caller-owned; must not be used by another call in flight.
+ *   workspace_bytes its size
+ *   stream         cudaStream_t
+ * bf16: D must be 64 or 128 and G <= 16.  The new token sees the whole
+ * cached prefix (no causal term).
+ */
+int gqa_decode(const void* q, const void* kcache, const void* vcache,
+               const int* cache_seqlens, void* out, int B, int Hq, int Hkv, int D,
+               float scale, int num_splits, int max_seqlen_k, int dtype,
+               void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gqa_device_status -- synchronises `stream`, then returns and clears the
+ * library's device error word for the current device: GQA_OK,
+ * GQA_ERR_DEVICE_BOUNDS or GQA_ERR_DEVICE_TIMEOUT (GQA_ERR_CUDA if the
+ * synchronisation itself failed).
+ */
+int gqa_device_status(void* stream);
+
+/* gqa_status_string -- static, human-readable name of a status code. */
+const char* gqa_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQA_H_ */

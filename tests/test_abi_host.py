@@ -1,0 +1,114 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load, export every function include/gqa.h declares, and
+reject bad arguments before touching the device (argument validation runs
+before any CUDA call, so fake device pointers are safe here).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import grouped_query_attention_08_b300 as gqa
+from grouped_query_attention_08_b300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return gqa.load_library()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "gqa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(gqa_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for n in ["gqa_fwd", "gqa_decode", "gqa_decode_workspace_bytes", "gqa_decode_num_splits",
+              "gqa_device_status", "gqa_status_string"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    assert gqa.gqa_status_string(0) == "GQA_OK"
+    assert gqa.gqa_status_string(1) == "GQA_ERR_INVALID_ARG"
+    assert gqa.gqa_status_string(5) == "GQA_ERR_DEVICE_BOUNDS"
+    assert gqa.gqa_status_string(99) == "GQA_ERR_UNKNOWN"
+
+
+FAKE = 0x10000   # 16-byte aligned, never dereferenced: validation fails first
+
+
+def _fwd(lib, B=1, Hq=4, Hkv=2, Sq=8, Sk=8, D=64, scale=0.125, causal=0, dtype=0, q=FAKE, k=FAKE,
+         v=FAKE, out=FAKE, lse=None, seqlens=None):
+    P = ctypes.c_void_p
+    return lib.gqa_fwd(P(q), P(k), P(v), P(out), P(lse) if lse else None, B, Hq, Hkv, Sq, Sk, D, scale,
+                       causal, P(seqlens) if seqlens else None, dtype, None)
+
+
+def test_fwd_rejects_indivisible_heads(lib):
+    assert _fwd(lib, Hq=6, Hkv=4) == gqa.GQA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Sq=0), dict(Sk=-1), dict(D=0), dict(Hkv=0),
+                                dict(q=0), dict(out=0), dict(scale=float("nan")),
+                                dict(scale=float("inf")), dict(causal=2), dict(dtype=7),
+                                dict(q=FAKE + 8), dict(lse=FAKE + 2), dict(seqlens=FAKE + 1)])
+def test_fwd_rejects_invalid_arguments(lib, kw):
+    assert _fwd(lib, **kw) == gqa.GQA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(D=96), dict(D=32), dict(D=256), dict(Hq=129, Hkv=1)])
+def test_fwd_bf16_unsupported_shapes(lib, kw):
+    assert _fwd(lib, **kw) == gqa.GQA_ERR_UNSUPPORTED
+
+
+def test_fwd_fp32_head_dim_limit(lib):
+    assert _fwd(lib, D=257, dtype=1) == gqa.GQA_ERR_UNSUPPORTED
+
+
+def _dec(lib, B=2, Hq=8, Hkv=2, D=128, scale=0.1, ns=1, smax=64, dtype=0, ws=None, wsb=0, q=FAKE,
+         lens=FAKE):
+    P = ctypes.c_void_p
+    return lib.gqa_decode(P(q), P(FAKE), P(FAKE), P(lens) if lens else None, P(FAKE), B, Hq, Hkv, D,
+                          scale, ns, smax, dtype, P(ws) if ws else None, wsb, None)
+
+
+def test_decode_validation(lib):
+    assert _dec(lib, Hq=6, Hkv=4) == gqa.GQA_ERR_INVALID_ARG
+    assert _dec(lib, lens=0) == gqa.GQA_ERR_INVALID_ARG
+    assert _dec(lib, smax=0) == gqa.GQA_ERR_INVALID_ARG
+    assert _dec(lib, ns=129) == gqa.GQA_ERR_INVALID_ARG
+    assert _dec(lib, D=96) == gqa.GQA_ERR_UNSUPPORTED
+    assert _dec(lib, Hq=32, Hkv=2) == gqa.GQA_ERR_UNSUPPORTED          # G = 16 > 8 on bf16
+    # two splits need a workspace
+    assert _dec(lib, ns=2) == gqa.GQA_ERR_INVALID_ARG
+    need = lib.gqa_decode_workspace_bytes(2, 8, 2, 128, 2, 64)
+    assert need > 0
+    assert _dec(lib, ns=2, ws=FAKE, wsb=need - 1) == gqa.GQA_ERR_INVALID_ARG
+    assert _dec(lib, ns=2, ws=FAKE + 4, wsb=need) == gqa.GQA_ERR_INVALID_ARG
+
+
+def test_split_planning(lib):
+    # explicit counts: split length = ceil(Smax / n) rounded up to 16 keys
+    assert gqa.gqa_decode_num_splits(4, 8, 8192, 1) == 1
+    assert gqa.gqa_decode_num_splits(4, 8, 8192, 8) == 8
+    assert gqa.gqa_decode_num_splits(4, 8, 100, 3) == 3          # ceil(100/3)=34 -> 48 -> 3 splits
+    assert gqa.gqa_decode_num_splits(4, 8, 100, 7) == 7          # 15 -> 16 -> 7 splits
+    assert gqa.gqa_decode_num_splits(4, 8, 40, 100) == 3         # at most one split per 16 keys
+    n = gqa.gqa_decode_num_splits(64, 8, 8192, 0)
+    assert 1 <= n <= 128
+    assert gqa.gqa_decode_workspace_bytes(64, 64, 8, 128, 1, 8192) == 0
+    ws = gqa.gqa_decode_workspace_bytes(64, 64, 8, 128, 8, 8192)
+    assert ws >= 64 * 64 * 8 * 129 * 4
