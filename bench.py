@@ -175,12 +175,26 @@ def cpu_baseline(workload, seconds=10.0):
             pairs += max(0, lim)
         return dt, 4 * w.D * pairs
 
-    dt, _ = run(256)
-    n = int(min(total, max(256, 256 * seconds / max(dt, 1e-3))))
-    dt, flops = run(n)
+    # grow the row sample until it takes about `seconds`; if the whole workload is
+    # faster than that, repeat it
+    n, dt = 1024, 0.0
+    while True:
+        dt, flops = run(n)
+        if dt >= 0.5 * seconds or n >= total:
+            break
+        n = int(min(total, max(2 * n, n * 0.7 * seconds / max(dt, 1e-3))))
+    reps = 1
+    if dt < 0.5 * seconds:
+        reps = int(max(1, round(seconds / max(dt, 1e-3))))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            run(n)
+        dt = time.perf_counter() - t0
+        flops *= reps
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": "%d of %d query rows of %s (fp64, OpenMP), %.1f s" % (n, total, workload, dt),
+            "sample": "%d of %d query rows of %s x %d repeat(s) (fp64 oracle, OpenMP), %.1f s" % (
+                n, total, workload, reps, dt),
             "seconds": dt}
 
 
@@ -219,7 +233,7 @@ def _workload_name(w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--prefill", default="bert_base",

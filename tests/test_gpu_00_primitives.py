@@ -27,7 +27,8 @@ def test_tma_swizzle_and_kmajor_mma(st):
     A = torch.randn(128, 64, generator=g).to(torch.bfloat16)
     B = torch.randn(128, 64, generator=g).to(torch.bfloat16)
     S = torch.zeros(128, 128, device="cuda")
-    rc = st.gqa_selftest_qk(A.cuda().data_ptr(), B.cuda().data_ptr(), S.data_ptr())
+    dA, dB = A.cuda(), B.cuda()          # keep the device copies alive across the call
+    rc = st.gqa_selftest_qk(dA.data_ptr(), dB.data_ptr(), S.data_ptr())
     assert rc == 0
     ref = A.double() @ B.double().T
     err = (S.cpu().double() - ref).abs().max().item()
@@ -40,12 +41,13 @@ def test_tmem_a_operand_and_mn_major_b(st, N):
     P = torch.rand(128, 128, generator=g)
     V = torch.randn(128, N, generator=g).to(torch.bfloat16)
     O = torch.zeros(128, N, device="cuda")
-    rc = st.gqa_selftest_pv(P.cuda().data_ptr(), V.cuda().data_ptr(), O.data_ptr(), N, 128 * 128, 1024)
+    dP, dV = P.cuda(), V.cuda()          # keep the device copies alive across the call
+    rc = st.gqa_selftest_pv(dP.data_ptr(), dV.data_ptr(), O.data_ptr(), N, 128 * 128, 1024)
     assert rc == 0
     ref = P.to(torch.bfloat16).double() @ V.double()
     err = (O.cpu().double() - ref).abs().max().item()
     if err >= 1e-3:  # diagnostic: try the other reading of the descriptor offsets
         O2 = torch.zeros(128, N, device="cuda")
-        st.gqa_selftest_pv(P.cuda().data_ptr(), V.cuda().data_ptr(), O2.data_ptr(), N, 1024, 128 * 128)
+        st.gqa_selftest_pv(dP.data_ptr(), dV.data_ptr(), O2.data_ptr(), N, 1024, 128 * 128)
         err2 = (O2.cpu().double() - ref).abs().max().item()
         pytest.fail("P.V via tcgen05 differs by %g (swapped LBO/SBO: %g)" % (err, err2))
