@@ -208,3 +208,30 @@ def gqa_device_status(stream=None) -> int:
     torch = _torch()
     st = stream if stream is not None else torch.cuda.current_stream()
     return int(load_library().gqa_device_status(ctypes.c_void_p(st.cuda_stream)))
+
+
+def gqa_decode_noalloc(q, kcache, vcache, cache_seqlens, *, scale=None, num_splits=0, out=None, stream=None):
+    """gqa_decode without a workspace argument, for callers that cannot allocate
+    device memory: the split partials go to the library's own fixed 32 MiB
+    device scratch array (see include/gqa.h).  Calls on one device share that
+    array, so calls that overlap on the GPU must be serialised by the caller.
+    Only ``out`` is allocated here when it is not given."""
+    torch = _torch()
+    lib = load_library()
+    fn = lib.gqa_decode_noalloc
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.restype = i32
+    fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, vp]
+    B, Hq, D = q.shape
+    _, Smax, Hkv, _ = kcache.shape
+    code = _dtype_code(q)
+    if out is None:
+        out = torch.empty_like(q)
+    dev = _check_cuda(q, kcache, vcache, cache_seqlens, out)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = fn(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_seqlens), _ptr(out), B, Hq, Hkv, D, float(scale),
+            int(num_splits), Smax, code, _stream(dev, stream))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_decode_noalloc")
+    return out

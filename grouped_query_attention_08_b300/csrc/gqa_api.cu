@@ -366,3 +366,49 @@ int gqa_device_status(void* stream) {
 }
 
 }  // extern "C"
+
+// ===================================================== no-allocation decode
+// A variant of gqa_decode for callers that cannot allocate device memory: the
+// split partials live in a fixed scratch array that belongs to the library.
+namespace {
+
+constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // 32 MiB per device
+
+// File-scope device array: every device that loads this library holds one
+// copy until the process exits.  In host code the name is only a stand-in
+// for the symbol; the device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {nullptr};
+
+// Device address of g_decode_scratch on device `dev` (which must be the
+// current device), looked up once per device and cached.
+void* static_scratch(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_decode_scratch) != cudaSuccess) return nullptr;
+    g_scratch_addr[dev] = p;
+  }
+  return g_scratch_addr[dev];
+}
+
+}  // namespace
+
+extern "C" int gqa_decode_noalloc(const void* q, const void* kcache, const void* vcache,
+                                  const int* cache_seqlens, void* out, int B, int Hq, int Hkv, int D,
+                                  float scale, int num_splits, int max_seqlen_k, int dtype, void* stream) {
+  const size_t need = gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, max_seqlen_k);
+  if (need > kStaticScratchBytes) return GQA_ERR_UNSUPPORTED;
+  void* ws = nullptr;
+  if (need > 0) {
+    ws = static_scratch(current_device());
+    if (!ws) return GQA_ERR_CUDA;
+  }
+  // Nothing in the scratch has to start at zero: every split partial the
+  // combine step reads is written earlier in the same call.
+  return gqa_decode(q, kcache, vcache, cache_seqlens, out, B, Hq, Hkv, D, scale, num_splits, max_seqlen_k,
+                    dtype, ws, need, stream);
+}

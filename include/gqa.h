@@ -149,6 +149,39 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache,
                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gqa_decode_noalloc -- gqa_decode for callers that cannot allocate device
+ * memory.  The pages have no counterpart to this entry point.
+ *
+ * Some callers only ever receive the input and output buffers -- an operator
+ * or plugin interface of a host framework that owns all device memory -- and
+ * others must not allocate on the decode path at all, because cudaMalloc can
+ * synchronise the device and takes unbounded time.  Those callers cannot
+ * provide gqa_decode's split workspace.  This entry point takes the same
+ * arguments as gqa_decode minus the workspace and puts the split partials in
+ * a scratch array of GQA_DECODE_NOALLOC_SCRATCH_BYTES (32 MiB) that the
+ * library holds in device memory: one file-scope device array per device that
+ * loads the library, kept until the process exits.  No call allocates or
+ * frees anything.
+ *
+ *   - Size limit: calls whose split partials would need more than 32 MiB
+ *     (gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, max_seqlen_k)
+ *     > GQA_DECODE_NOALLOC_SCRATCH_BYTES) return GQA_ERR_UNSUPPORTED and
+ *     enqueue nothing; lower num_splits or use gqa_decode.
+ *   - Set-up: the first call on a device looks up the scratch array's
+ *     device address (once per device, with that device current).  Make that
+ *     first call before any stream capture on the device.
+ *   - Sharing: every call on a device uses the same scratch array, which
+ *     keeps the previous call's contents (nothing in it has to start at zero).
+ *     Calls that overlap on the GPU -- on different streams, or from several
+ *     host threads -- race on it; serialise them.
+ *   - Everything else (arguments, layouts, errors) is as for gqa_decode.
+ */
+#define GQA_DECODE_NOALLOC_SCRATCH_BYTES (32u << 20)
+int gqa_decode_noalloc(const void* q, const void* kcache, const void* vcache,
+                       const int* cache_seqlens, void* out, int B, int Hq, int Hkv, int D,
+                       float scale, int num_splits, int max_seqlen_k, int dtype, void* stream);
+
+/*
  * gqa_device_status -- synchronises `stream`, then returns and clears the
  * library's device error word for the current device: GQA_OK,
  * GQA_ERR_DEVICE_BOUNDS or GQA_ERR_DEVICE_TIMEOUT (GQA_ERR_CUDA if the
