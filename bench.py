@@ -43,10 +43,14 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 # source is unchanged (sha256 of the file below).  Filled from the committed
 # profiles/*.md summaries; None = not captured for the current source.
 NCU_TRAFFIC = {
-    "prefill": {"source": "grouped_query_attention_08_b300/csrc/prefill_sm103.cuh", "sha256": None,
-                "workload": "bert_base", "bytes": None},
-    "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh", "sha256": None,
-               "workload": "llama_decode", "bytes": None},
+    # profiles/prefill_kernel_d64_bert_base.md (one launch, bert_base)
+    "prefill": {"source": "grouped_query_attention_08_b300/csrc/prefill_sm103.cuh",
+                "sha256": "c2e4626c5d03741fde20f8eaee84facd1726816a706742e5e2815e3b4d8bb501",
+                "workload": "bert_base", "bytes": 91089664},
+    # profiles/decode_split_kernel_llama_decode_small.md (B=16 capture scaled to B=64 by KV bytes)
+    "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh",
+               "sha256": "1929d6fc61ce89c8eaa65031eb85b9fa679bfa8a328507b3a713dd2f30cf1f18",
+               "workload": "llama_decode", "bytes": 1269700000},
 }
 
 
@@ -149,75 +153,95 @@ def _max_over_ranks(x, ws, device):
     return float(t.item())
 
 
+class OracleSampler:
+    """Times the fp64 oracle (as it stands) on row samples of a prefill workload."""
+
+    def __init__(self, workload):
+        import numpy as np
+        import oracle
+        self.oracle = oracle
+        self.w = w = inputs.WORKLOADS[workload]
+        inp = inputs.make_workload(w)
+        self.q = inp["q"].float().numpy()
+        self.k = inp["k"].float().numpy()
+        self.v = inp["v"].float().numpy()
+        self.lens = None if inp["seqlens_k"] is None else inp["seqlens_k"].numpy()
+        self.total = w.B * w.Hq * w.Sq
+        oracle.build()
+        # admissible keys of every (b, h, i) row, for the flop count of a sample
+        i = np.arange(w.Sq)
+        Lb = np.full(w.B, w.Sk) if self.lens is None else self.lens.astype(np.int64)
+        lim = Lb[:, None] + 0 * i[None, :]
+        if w.causal:
+            lim = np.minimum(lim, i[None, :] + w.Sk - w.Sq + 1)
+        lim = np.maximum(lim, 0)                                    # [B, Sq]
+        self.row_keys = np.broadcast_to(lim[:, None, :], (w.B, w.Hq, w.Sq)).reshape(-1)
+
+    def rows(self, n, seed=12345):
+        return inputs.sample_rows(self.total, n, seed).numpy()
+
+    def run(self, rows):
+        """Returns (seconds, algorithmic flops) of one oracle call on these rows."""
+        w = self.w
+        t0 = time.perf_counter()
+        self.oracle.attention(self.q, self.k, self.v, scale=w.scale, causal=w.causal, seqlens_k=self.lens,
+                              rows=rows)
+        dt = time.perf_counter() - t0
+        return dt, 4 * w.D * int(self.row_keys[rows].sum())
+
+    def calibrate(self, seconds):
+        """Row count whose oracle call takes about `seconds` (capped at the whole workload)."""
+        n = 256
+        while True:
+            dt, _ = self.run(self.rows(n))
+            if dt >= 0.5 * seconds or n >= self.total:
+                return n, dt
+            n = int(min(self.total, max(2 * n, n * 0.8 * seconds / max(dt, 1e-4))))
+
+
 def cpu_baseline(workload, seconds=10.0):
-    """Time the fp64 oracle (as it stands) on a bounded row sample of the workload."""
-    import oracle
-    w = inputs.WORKLOADS[workload]
-    inp = inputs.make_workload(w)
-    q = inp["q"].float().numpy()
-    k = inp["k"].float().numpy()
-    v = inp["v"].float().numpy()
-    lens = None if inp["seqlens_k"] is None else inp["seqlens_k"].numpy()
-    total = w.B * w.Hq * w.Sq
-    oracle.build()
-
-    def run(n):
-        rows = inputs.sample_rows(total, n, 12345).numpy()
-        t0 = time.perf_counter()
-        oracle.attention(q, k, v, scale=w.scale, causal=w.causal, seqlens_k=lens, rows=rows)
-        dt = time.perf_counter() - t0
-        pairs = 0
-        for r in rows:
-            i = r % w.Sq
-            b = r // (w.Sq * w.Hq)
-            Lb = w.Sk if lens is None else int(lens[b])
-            lim = min(Lb, i + w.Sk - w.Sq + 1) if w.causal else Lb
-            pairs += max(0, lim)
-        return dt, 4 * w.D * pairs
-
-    # grow the row sample until it takes about `seconds`; if the whole workload is
-    # faster than that, repeat it
-    n, dt = 1024, 0.0
-    while True:
-        dt, flops = run(n)
-        if dt >= 0.5 * seconds or n >= total:
-            break
-        n = int(min(total, max(2 * n, n * 0.7 * seconds / max(dt, 1e-3))))
-    reps = 1
-    if dt < 0.5 * seconds:
-        reps = int(max(1, round(seconds / max(dt, 1e-3))))
-        t0 = time.perf_counter()
-        for _ in range(reps):
-            run(n)
-        dt = time.perf_counter() - t0
-        flops *= reps
+    """The oracle timed on the host cores on a bounded sample (about `seconds` of work)."""
+    o = OracleSampler(workload)
+    n, dt = o.calibrate(seconds)
+    rows = o.rows(n)
+    reps = 1 if dt >= 0.5 * seconds else int(max(1, round(seconds / max(dt, 1e-4))))
+    tot_t, tot_f = 0.0, 0
+    for _ in range(reps):
+        t, f = o.run(rows)
+        tot_t += t
+        tot_f += f
     cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+    return {"value": tot_f / tot_t / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
             "sample": "%d of %d query rows of %s x %d repeat(s) (fp64 oracle, OpenMP), %.1f s" % (
-                n, total, workload, reps, dt),
-            "seconds": dt}
+                n, o.total, workload, reps, tot_t)}
 
 
 def run_reference(args):
+    """The oracle as the reference arm: every step is one oracle call on a row
+    sample sized so that the whole warm-up + timed run takes about two minutes."""
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
     w = inputs.WORKLOADS[args.prefill]
-    res = []
+    o = OracleSampler(args.prefill)
+    per_step = max(0.02, 120.0 / (args.steps + args.warmup))
+    n, _ = o.calibrate(per_step)
+    rows = o.rows(n)
     for _ in range(args.warmup):
-        cpu_baseline(args.prefill, seconds=2.0)
-    t0 = time.perf_counter()
+        o.run(rows)
+    tot_t, tot_f = 0.0, 0
     for _ in range(args.steps):
-        res.append(cpu_baseline(args.prefill, seconds=5.0))
-    wall = time.perf_counter() - t0
-    val = statistics.median([r["value"] for r in res])
-    cb = dict(res[-1])
-    cb["value"] = val
-    cb.pop("seconds", None)
+        t, f = o.run(rows)
+        tot_t += t
+        tot_f += f
+    val = tot_f / tot_t / 1e12
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    cb = {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+          "sample": "%d of %d query rows of %s per step (fp64 oracle, OpenMP)" % (n, o.total, args.prefill)}
     line = {"impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": ws,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": wall * 1e3 / max(1, args.steps),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t * 1e3 / max(1, args.steps),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": {"workload": _workload_name(w), "sampled": True},
+            "data": "synthetic", "config": {"workload": _workload_name(w), "sampled_rows_per_step": n},
             "cpu_baseline": cb,
             "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
@@ -381,7 +405,6 @@ def main():
     cb = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(args.prefill)
-        cb.pop("seconds", None)
 
     launches_per_step = 1 + 1 + (1 if nsplit > 1 else 0)
     if rank == 0:

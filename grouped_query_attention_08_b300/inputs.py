@@ -67,6 +67,8 @@ WORKLOADS = {
                                        "bf16", 2),
     # Llama-style 64/8-head decode over a cache with lengths U[1024,8192]
     "llama_decode": DecodeWorkload("llama_decode", 64, 64, 8, 128, 8192, (1024, 8192), "bf16", 3),
+    # the same decode shapes with a quarter of the batch (smaller device footprint for profiling)
+    "llama_decode_small": DecodeWorkload("llama_decode_small", 16, 64, 8, 128, 8192, (1024, 8192), "bf16", 3),
     # long causal prefill, D=128
     "causal_long": PrefillWorkload("causal_long", 4, 32, 8, 8192, 8192, 128, True, None, "bf16", 4),
 }
