@@ -113,8 +113,11 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   const int G = Hq / Hkv;
   const int Mq = pf::kBM / G;
   const long long n_qblk = (Sq + pf::kNQT * Mq - 1) / (pf::kNQT * Mq);
-  const long long grid = n_qblk * B * Hkv;
-  if (grid <= 0 || grid > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  const long long n_units = n_qblk * B * Hkv;
+  if (n_units <= 0 || n_units > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  // persistent grid: one CTA per SM (the kernel's shared memory and register
+  // use allow no more), each looping over work units
+  const long long grid = std::min<long long>(n_units, num_sms(current_device()));
   CUtensorMap tmQ, tmK, tmV;
   if (!encode_4d_bf16(&tmQ, q, D, Hq, Sq, B, 64, G, Mq, 1) || !encode_4d_bf16(&tmK, k, D, Hkv, Sk, B, 64, 1, 128, 1) ||
       !encode_4d_bf16(&tmV, v, D, Hkv, Sk, B, 64, 1, 128, 1))
@@ -132,6 +135,7 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   p.Sk = Sk;
   p.Mq = Mq;
   p.n_qblk = int(n_qblk);
+  p.n_units = int(n_units);
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.timeout_ns = wait_timeout_ns();

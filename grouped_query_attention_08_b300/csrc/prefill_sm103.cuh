@@ -1,5 +1,6 @@
 // prefill_sm103.cuh -- bf16 grouped-query attention forward (prefill) for
-// sm_103a: TMA + tcgen05.mma with TMEM accumulators, warp-specialised.
+// sm_103a: TMA + tcgen05.mma with TMEM accumulators, warp-specialised and
+// persistent.
 //
 // Method (sources cited by page title and section):
 //  * "3个GQA核心优化技巧" (blog.gitcode.com), "GQA的分组共享机制" and
@@ -14,18 +15,25 @@
 //    softmax) and never written to global memory; "V3 ve donanım uyumu":
 //    producer warps move data while consumer warps compute.
 //
-// CTA work unit: batch b, K/V head kvh, and 2 consecutive Q tiles of Mq =
-// floor(128/G) tokens x G heads each.  Warp roles (384 threads):
-//   warps 0-3  softmax for Q tile 0 (thread = one row = one TMEM lane)
-//   warps 4-7  softmax for Q tile 1
-//   warp  8    TMA producer: Q tiles once, then a K ring and a V ring
+// Work unit: batch b, K/V head kvh, and 2 consecutive Q tiles of Mq =
+// floor(128/G) tokens x G heads each.  The grid is persistent (at most one
+// CTA per SM); CTA c takes units c, c + gridDim.x, ...  Causal launches
+// number the units longest first.  Warp roles (384 threads):
+//   warps 0-3  softmax + epilogue for Q tile 0 (thread = one row = one TMEM lane)
+//   warps 4-7  softmax + epilogue for Q tile 1
+//   warp  8    TMA producer: the unit's Q tiles, then a K ring and a V ring
 //   warp  9    MMA issuer: S_t = Q_t K^T into TMEM, O_t += P_t V with P_t
 //              read from TMEM (P overwrites S_t as packed bf16)
 //   warps 10-11 idle (they complete the third warpgroup, which hands its
 //              registers to the softmax warpgroups with setmaxnreg)
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
 // The two softmax warpgroups ping-pong: while one computes exponentials the
-// tensor core runs the other's PV and next QK^T.
+// tensor core runs the other's PV and next QK^T.  Across units, the MMA warp
+// starts the next unit's QK^T while the softmax warps are still writing the
+// previous unit's output (S and O are separate TMEM regions); only the first
+// PV of a unit waits for the previous epilogue to have read O_t.  With D = 64
+// the Q tiles are double-buffered so the next unit's Q lands during the
+// current one.
 //
 // Softmax details: t = s * scale * log2(e); the running max m is only moved
 // when a tile's max exceeds it by more than 8 (log2 units); otherwise the
@@ -41,7 +49,7 @@ namespace prefill {
 
 constexpr int kBM = 128;       // rows per Q tile (= TMEM lanes)
 constexpr int kBN = 128;       // keys per K/V tile
-constexpr int kNQT = 2;        // Q tiles per CTA
+constexpr int kNQT = 2;        // Q tiles per work unit
 constexpr int kWarpTMA = 8;
 constexpr int kWarpMMA = 9;
 constexpr int kThreads = 384;
@@ -54,14 +62,17 @@ template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;                    // 64-column (128-byte) halves of a row
   static constexpr int kStages = (D == 64) ? 3 : 2;         // depth of the K ring and of the V ring
+  static constexpr int kQBufs = (D == 64) ? 2 : 1;          // Q tile sets in flight
   static constexpr uint32_t kHalfBytes = 128u * 128u;       // 128 rows x 128 bytes
   static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;
+  static constexpr uint32_t kQSetBytes = kNQT * kTileBytes;
   static constexpr uint32_t kOffQ = 0;
-  static constexpr uint32_t kOffK = kOffQ + kNQT * kTileBytes;
+  static constexpr uint32_t kOffK = kOffQ + kQBufs * kQSetBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // barriers: q_full, k_full[S], k_empty[S], v_full[S], v_empty[S], s_full[2], p_full[2], o_done[2], drain
-  static constexpr int kNumBars = 1 + 4 * kStages + 3 * kNQT + 1;
+  // barriers: q_full[QB], q_empty[QB], k_full[S], k_empty[S], v_full[S], v_empty[S],
+  //           s_full[2], p_full[2], o_done[2], o_free[2], drain
+  static constexpr int kNumBars = 2 * kQBufs + 4 * kStages + 4 * kNQT + 1;
   static constexpr uint32_t kOffTmemSlot = kOffBar + 8u * kNumBars;
   static constexpr uint32_t kOffAbort = kOffTmemSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
@@ -83,10 +94,37 @@ struct Params {
   int B, Hq, Hkv, G, Sq, Sk;
   int Mq;                 // tokens per Q tile (G * Mq <= 128)
   int n_qblk;             // ceil(Sq / (kNQT * Mq))
+  int n_units;            // n_qblk * B * Hkv
   int causal;
   float scale_log2;       // scale * log2(e)
   unsigned long long timeout_ns;
 };
+
+struct Unit {
+  int b, kvh, q0, Lb, n_tiles;
+  bool bad_len;
+};
+
+// Work unit u -> (b, kvh, first token, key length, number of key tiles).
+DEVI Unit unit_info(const Params& p, int u) {
+  Unit U;
+  const int bh_count = p.B * p.Hkv;
+  int qblk = u / bh_count;
+  if (p.causal) qblk = p.n_qblk - 1 - qblk;     // longest units first
+  const int bh = u % bh_count;
+  U.b = bh / p.Hkv;
+  U.kvh = bh % p.Hkv;
+  U.q0 = qblk * kNQT * p.Mq;
+  int Lb = p.seqlens ? __ldg(p.seqlens + U.b) : p.Sk;
+  U.bad_len = (Lb < 0 || Lb > p.Sk);
+  if (U.bad_len) Lb = 0;
+  U.Lb = Lb;
+  const int q_last = min(U.q0 + kNQT * p.Mq, p.Sq) - 1;
+  int kmax = Lb;
+  if (p.causal) kmax = min(kmax, q_last + p.Sk - p.Sq + 1);
+  U.n_tiles = kmax > 0 ? (kmax + kBN - 1) / kBN : 0;
+  return U;
+}
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -94,47 +132,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tmV, const Params p) {
   using L = Layout<D>;
   constexpr int S = L::kStages;
+  constexpr int QB = L::kQBufs;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* sbase = smem_raw + (base - raw_addr);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-
-  // ---- work unit: causal launches take the longest (last) q blocks first
-  const int bh_count = p.B * p.Hkv;
-  int qblk = blockIdx.x / bh_count;
-  if (p.causal) qblk = p.n_qblk - 1 - qblk;
-  const int bh = blockIdx.x % bh_count;
-  const int b = bh / p.Hkv;
-  const int kvh = bh % p.Hkv;
-  const int q0 = qblk * kNQT * p.Mq;
   const int rows_per_tile = p.G * p.Mq;
 
-  int Lb = p.seqlens ? p.seqlens[b] : p.Sk;
-  const bool bad_len = (Lb < 0 || Lb > p.Sk);
-  if (bad_len) Lb = 0;
-  const int q_last = min(q0 + kNQT * p.Mq, p.Sq) - 1;
-  int kmax = Lb;
-  if (p.causal) kmax = min(kmax, q_last + p.Sk - p.Sq + 1);
-  const int n_tiles = kmax > 0 ? (kmax + kBN - 1) / kBN : 0;
-
   auto bar = [&](int i) -> uint32_t { return base + L::kOffBar + 8u * uint32_t(i); };
-  const uint32_t q_full = bar(0);
-  auto k_full = [&](int s) { return bar(1 + s); };
-  auto k_empty = [&](int s) { return bar(1 + S + s); };
-  auto v_full = [&](int s) { return bar(1 + 2 * S + s); };
-  auto v_empty = [&](int s) { return bar(1 + 3 * S + s); };
-  auto s_full = [&](int t) { return bar(1 + 4 * S + t); };
-  auto p_full = [&](int t) { return bar(1 + 4 * S + kNQT + t); };
-  auto o_done = [&](int t) { return bar(1 + 4 * S + 2 * kNQT + t); };
-  const uint32_t drain = bar(1 + 4 * S + 3 * kNQT);
+  auto q_full = [&](int i) { return bar(i); };
+  auto q_empty = [&](int i) { return bar(QB + i); };
+  auto k_full = [&](int s) { return bar(2 * QB + s); };
+  auto k_empty = [&](int s) { return bar(2 * QB + S + s); };
+  auto v_full = [&](int s) { return bar(2 * QB + 2 * S + s); };
+  auto v_empty = [&](int s) { return bar(2 * QB + 3 * S + s); };
+  auto s_full = [&](int t) { return bar(2 * QB + 4 * S + t); };
+  auto p_full = [&](int t) { return bar(2 * QB + 4 * S + kNQT + t); };
+  auto o_done = [&](int t) { return bar(2 * QB + 4 * S + 2 * kNQT + t); };
+  auto o_free = [&](int t) { return bar(2 * QB + 4 * S + 3 * kNQT + t); };
+  const uint32_t drain = bar(2 * QB + 4 * S + 4 * kNQT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffTmemSlot);
   const uint64_t to = p.timeout_ns;
 
   if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
+    for (int i = 0; i < QB; ++i) {
+      mbar_init(q_full(i), 1);
+      mbar_init(q_empty(i), 1);
+    }
     for (int s = 0; s < S; ++s) {
       mbar_init(k_full(s), 1);
       mbar_init(k_empty(s), 1);
@@ -145,10 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(s_full(t), 1);
       mbar_init(p_full(t), 128);
       mbar_init(o_done(t), 1);
+      mbar_init(o_free(t), 128);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
-    if (bad_len) raise_error(kErrBounds);
     fence_mbar_init();
     fence_proxy_async_smem();
   }
@@ -170,48 +197,67 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n_tiles > 0) {
-      int issued = 0;
+    if (lane == 0) {
+      uint32_t kv_it = 0;       // K/V tiles issued so far (ring position)
+      uint32_t qn = 0;          // units with work so far (Q buffer position)
       bool ok = true;
+      bool k_only = false;
       const uint32_t q_bytes = uint32_t(kNQT * L::kHalves * 64 * 2 * rows_per_tile);
-      mbar_arrive_expect_tx(q_full, q_bytes);
-      for (int t = 0; t < kNQT; ++t)
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_4d(base + L::kOffQ + t * L::kTileBytes + h * L::kHalfBytes, &tmQ, q_full, h * 64,
-                      kvh * p.G, q0 + t * p.Mq, b);
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int s = j % S;
-        const uint32_t ph = (j / S) & 1;
-        ok = mbar_wait(k_empty(s), ph ^ 1, abort_flag, to);
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const Unit U = unit_info(p, u);
+        if (U.bad_len) raise_error(kErrBounds);
+        if (U.n_tiles == 0) continue;
+        const int qb = int(qn % QB);
+        ok = mbar_wait(q_empty(qb), ((qn / QB) & 1) ^ 1, abort_flag, to);
         if (!ok) break;
-        mbar_arrive_expect_tx(k_full(s), L::kTileBytes);
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_4d(base + L::kOffK + s * L::kTileBytes + h * L::kHalfBytes, &tmK, k_full(s), h * 64,
-                      kvh, j * kBN, b);
-        ok = mbar_wait(v_empty(s), ph ^ 1, abort_flag, to);
-        if (!ok) break;
-        mbar_arrive_expect_tx(v_full(s), L::kTileBytes);
-        for (int h = 0; h < L::kHalves; ++h)
-          tma_load_4d(base + L::kOffV + s * L::kTileBytes + h * L::kHalfBytes, &tmV, v_full(s), h * 64,
-                      kvh, j * kBN, b);
-        issued = j + 1;
+        mbar_arrive_expect_tx(q_full(qb), q_bytes);
+        for (int t = 0; t < kNQT; ++t)
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_4d(base + L::kOffQ + qb * L::kQSetBytes + t * L::kTileBytes + h * L::kHalfBytes, &tmQ,
+                        q_full(qb), h * 64, U.kvh * p.G, U.q0 + t * p.Mq, U.b);
+        ++qn;
+        for (int j = 0; j < U.n_tiles; ++j) {
+          const int s = int(kv_it % S);
+          const uint32_t ph = (kv_it / S) & 1;
+          ok = mbar_wait(k_empty(s), ph ^ 1, abort_flag, to);
+          if (!ok) break;
+          mbar_arrive_expect_tx(k_full(s), L::kTileBytes);
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_4d(base + L::kOffK + s * L::kTileBytes + h * L::kHalfBytes, &tmK, k_full(s), h * 64,
+                        U.kvh, j * kBN, U.b);
+          ok = mbar_wait(v_empty(s), ph ^ 1, abort_flag, to);
+          if (!ok) {
+            k_only = true;     // K of ring position kv_it is in flight, V is not
+            break;
+          }
+          mbar_arrive_expect_tx(v_full(s), L::kTileBytes);
+          for (int h = 0; h < L::kHalves; ++h)
+            tma_load_4d(base + L::kOffV + s * L::kTileBytes + h * L::kHalfBytes, &tmV, v_full(s), h * 64,
+                        U.kvh, j * kBN, U.b);
+          ++kv_it;
+        }
       }
       if (!ok) {
-        // aborted: let the copies already in flight land before the CTA exits
+        // aborted: let the copies already in flight land before the CTA exits.
+        // Each waited phase belongs to the last load issued into its buffer,
+        // so it completes (or has completed) exactly once.
         volatile int no_abort = 0;
-        for (int j = max(0, issued - S); j < issued; ++j) {
-          mbar_wait(k_full(j % S), (j / S) & 1, &no_abort, 200000000ull);
-          mbar_wait(v_full(j % S), (j / S) & 1, &no_abort, 200000000ull);
+        const uint32_t first = kv_it > uint32_t(S) ? kv_it - S : 0u;
+        for (uint32_t it = first; it < kv_it; ++it) {
+          mbar_wait(k_full(int(it % S)), (it / S) & 1, &no_abort, 200000000ull);
+          mbar_wait(v_full(int(it % S)), (it / S) & 1, &no_abort, 200000000ull);
         }
+        if (k_only) mbar_wait(k_full(int(kv_it % S)), (kv_it / S) & 1, &no_abort, 200000000ull);
+        if (qn > 0) mbar_wait(q_full(int((qn - 1) % QB)), ((qn - 1) / QB) & 1, &no_abort, 200000000ull);
       }
     }
   } else if (warp == kWarpMMA) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && n_tiles > 0) {
+    if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(128, kBN, 0, 0);   // Q, K both K-major
       const uint32_t idesc_o = make_idesc_bf16(128, D, 0, 1);     // P (TMEM), V MN-major
-      auto issue_s = [&](int t, int s) {
-        const uint32_t qa = base + L::kOffQ + t * L::kTileBytes;
+      auto issue_s = [&](int t, int qb, int s) {
+        const uint32_t qa = base + L::kOffQ + qb * L::kQSetBytes + t * L::kTileBytes;
         const uint32_t ka = base + L::kOffK + s * L::kTileBytes;
         const uint32_t dst = tmem + (t ? L::kTmS1 : L::kTmS0);
 #pragma unroll
@@ -231,38 +277,55 @@ __global__ void __launch_bounds__(kThreads, 1)
                   idesc_o, (acc || ks > 0) ? 1u : 0u);
         }
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, to) && mbar_wait(k_full(0), 0, abort_flag, to);
-      if (ok) {
+      uint32_t kv_it = 0;       // K/V tiles consumed so far
+      uint32_t g_tile = 0;      // key tiles of earlier units (s_full / p_full phases)
+      uint32_t qn = 0;          // units with work so far
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const Unit U = unit_info(p, u);
+        if (U.n_tiles == 0) continue;
+        const int qb = int(qn % QB);
+        const int s0 = int(kv_it % S);
+        ok = mbar_wait(q_full(qb), (qn / QB) & 1, abort_flag, to) &&
+             mbar_wait(k_full(s0), (kv_it / S) & 1, abort_flag, to);
+        if (!ok) break;
         tc_fence_after();
         for (int t = 0; t < kNQT; ++t) {
-          issue_s(t, 0);
+          issue_s(t, qb, s0);
           umma_commit(s_full(t));
         }
-        umma_commit(k_empty(0));
-      }
-      for (int j = 0; ok && j < n_tiles; ++j) {
-        const int s = j % S;
-        const uint32_t ph = (j / S) & 1;
-        const int nj = j + 1;
-        const bool has_next = nj < n_tiles;
-        const int ns = nj % S;
-        const uint32_t nph = (nj / S) & 1;
-        ok = mbar_wait(v_full(s), ph, abort_flag, to);
-        if (ok && has_next) ok = mbar_wait(k_full(ns), nph, abort_flag, to);
-        for (int t = 0; ok && t < kNQT; ++t) {
-          ok = mbar_wait(p_full(t), j & 1, abort_flag, to);
-          if (!ok) break;
-          tc_fence_after();
-          issue_pv(t, s, j > 0);
-          umma_commit(o_done(t));
-          if (has_next) {
-            issue_s(t, ns);
-            umma_commit(s_full(t));
+        umma_commit(k_empty(s0));
+        if (U.n_tiles == 1) umma_commit(q_empty(qb));
+        for (int j = 0; ok && j < U.n_tiles; ++j) {
+          const uint32_t it = kv_it + j;
+          const int s = int(it % S);
+          const uint32_t ph = (it / S) & 1;
+          const bool has_next = j + 1 < U.n_tiles;
+          const int ns = int((it + 1) % S);
+          const uint32_t nph = ((it + 1) / S) & 1;
+          ok = mbar_wait(v_full(s), ph, abort_flag, to);
+          if (ok && has_next) ok = mbar_wait(k_full(ns), nph, abort_flag, to);
+          for (int t = 0; ok && t < kNQT; ++t) {
+            ok = mbar_wait(p_full(t), (g_tile + j) & 1, abort_flag, to);
+            // the unit's first PV overwrites O_t: the previous epilogue must have read it
+            if (ok && j == 0 && qn > 0) ok = mbar_wait(o_free(t), (qn - 1) & 1, abort_flag, to);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(t, s, j > 0);
+            if (!has_next) umma_commit(o_done(t));
+            if (has_next) {
+              issue_s(t, qb, ns);
+              umma_commit(s_full(t));
+            }
           }
+          if (!ok) break;
+          umma_commit(v_empty(s));
+          if (has_next) umma_commit(k_empty(ns));
+          if (j + 2 == U.n_tiles) umma_commit(q_empty(qb));   // the unit's last QK^T is issued
         }
-        if (!ok) break;
-        umma_commit(v_empty(s));
-        if (has_next) umma_commit(k_empty(ns));
+        kv_it += U.n_tiles;
+        g_tile += U.n_tiles;
+        ++qn;
       }
       if (!ok) {
         // aborted: wait for the tensor core to finish what was issued
@@ -281,147 +344,194 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = uint32_t(wq * 32) << 16;
     const uint32_t tS = tmem + lane_base + (t ? L::kTmS1 : L::kTmS0);
     const uint32_t tO = tmem + lane_base + (t ? L::kTmO1 : L::kTmO0);
-    const int token = q0 + t * p.Mq + r / p.G;
     const int g = r % p.G;
-    const bool row_ok = (r < rows_per_tile) && (token < p.Sq);
-    int limit = 0;
-    if (row_ok) {
-      limit = Lb;
-      if (p.causal) limit = min(limit, token + p.Sk - p.Sq + 1);
-      limit = max(limit, 0);
-    }
     const float c = p.scale_log2;
-    float m = -INFINITY;
-    float l = 0.f;
+    const uint64_t c2 = f2_pack(c, c);
+    uint32_t g_tile = 0;
+    uint32_t qn = 0;
     bool aborted = false;
 
-    for (int j = 0; j < n_tiles; ++j) {
-      bool ok = mbar_wait(s_full(t), j & 1, abort_flag, to);
-      if (ok && j > 0) ok = mbar_wait(o_done(t), (j - 1) & 1, abort_flag, to);
-      if (!__all_sync(0xffffffffu, ok)) {
-        aborted = true;
-        break;
+    for (int u = blockIdx.x; !aborted && u < p.n_units; u += gridDim.x) {
+      const Unit U = unit_info(p, u);
+      const int token = U.q0 + t * p.Mq + r / p.G;
+      const bool row_ok = (r < rows_per_tile) && (token < p.Sq);
+      int limit = 0;
+      if (row_ok) {
+        limit = U.Lb;
+        if (p.causal) limit = min(limit, token + p.Sk - p.Sq + 1);
+        limit = max(limit, 0);
       }
-      tc_fence_after();
-      uint32_t sv[kBN];
-      tmem_ld_32x32b_x32(tS + 0, sv + 0);
-      tmem_ld_32x32b_x32(tS + 32, sv + 32);
-      tmem_ld_32x32b_x32(tS + 64, sv + 64);
-      tmem_ld_32x32b_x32(tS + 96, sv + 96);
-      tmem_ld_wait_x128(sv);
+      float m = -INFINITY;
+      float l = 0.f;
 
-      const int lim = limit - j * kBN;
-      const bool full_tile = lim >= kBN;
-      float mt;
-      if (full_tile) {
-        // every key of the tile is admissible for this row
-        float e0 = __uint_as_float(sv[0]), e1 = e0;
-        if (c >= 0.f) {
+      for (int j = 0; j < U.n_tiles; ++j) {
+        const bool ok = mbar_wait(s_full(t), (g_tile + j) & 1, abort_flag, to);
+        if (!__all_sync(0xffffffffu, ok)) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[kBN];
+        tmem_ld_32x32b_x32(tS + 0, sv + 0);
+        tmem_ld_32x32b_x32(tS + 32, sv + 32);
+        tmem_ld_32x32b_x32(tS + 64, sv + 64);
+        tmem_ld_32x32b_x32(tS + 96, sv + 96);
+        tmem_ld_wait_x128(sv);
+
+        const int lim = limit - j * kBN;
+        // every key of the tile admissible for every row of the warp and a
+        // positive scale: take the max of the raw scores and fold the scale
+        // into the exponent's FMA.  The choice is warp-uniform because both
+        // branches end in tcgen05.st, which the whole warp must execute together.
+        const bool fast = __all_sync(0xffffffffu, lim >= kBN) && (c > 0.f);
+        float mt;
+        if (fast) {
+          float a0 = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+          float a1 = fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
+          float a2 = fmax3(__uint_as_float(sv[6]), __uint_as_float(sv[7]), __uint_as_float(sv[8]));
+          float a3 = fmax3(__uint_as_float(sv[9]), __uint_as_float(sv[10]), __uint_as_float(sv[11]));
 #pragma unroll
-          for (int i = 1; i < kBN; i += 2) {
-            e0 = fmaxf(e0, __uint_as_float(sv[i]));
-            if (i + 1 < kBN) e1 = fmaxf(e1, __uint_as_float(sv[i + 1]));
+          for (int i = 12; i < 124; i += 8) {
+            a0 = fmax3(a0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+            a1 = fmax3(a1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
+            a2 = fmax3(a2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
+            a3 = fmax3(a3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
+          }
+          a0 = fmax3(a0, __uint_as_float(sv[124]), __uint_as_float(sv[125]));
+          a1 = fmax3(a1, __uint_as_float(sv[126]), __uint_as_float(sv[127]));
+          mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c;
+        } else {
+          // edge tile (or non-positive scale): scale, mask, keep the scaled values
+          mt = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < kBN; ++i) {
+            const float f = (i < lim) ? __uint_as_float(sv[i]) * c : -INFINITY;
+            sv[i] = __float_as_uint(f);
+            mt = fmaxf(mt, f);
+          }
+        }
+        const float m_new = fmaxf(m, mt);
+        const bool need = m_new > m + kRescaleThreshold;
+        float alpha = 1.f;
+        if (need) {
+          alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+          l *= alpha;
+          m = m_new;
+        }
+        if (__any_sync(0xffffffffu, need && j > 0)) {
+          // move O_t to the new reference maximum.  The previous PV has
+          // completed: this tile's S was committed after it.
+#pragma unroll
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tO + cc, o);
+            tmem_ld_wait_x32(o);
+            const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+              const uint64_t v = f2_fma(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2, 0ull);
+              float lo, hi;
+              f2_unpack(v, lo, hi);
+              o[i] = __float_as_uint(lo);
+              o[i + 1] = __float_as_uint(hi);
+            }
+            tmem_st_32x32b_x32(tO + cc, o);
+          }
+        }
+        const float mref = (m == -INFINITY) ? 0.f : m;
+        uint64_t acc0 = 0ull, acc1 = 0ull;       // packed (+0.0f, +0.0f)
+        if (fast) {
+          const uint64_t nm2 = f2_pack(-mref, -mref);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int k0 = q * 32 + 2 * i;
+              float x0, x1;
+              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), c2, nm2), x0, x1);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              if (i & 1)
+                acc1 = f2_add(acc1, f2_pack(p0, p1));
+              else
+                acc0 = f2_add(acc0, f2_pack(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
           }
         } else {
 #pragma unroll
-          for (int i = 1; i < kBN; i += 2) {
-            e0 = fminf(e0, __uint_as_float(sv[i]));
-            if (i + 1 < kBN) e1 = fminf(e1, __uint_as_float(sv[i + 1]));
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int k0 = q * 32 + 2 * i;
+              const float p0 = ex2_approx(__uint_as_float(sv[k0]) - mref);
+              const float p1 = ex2_approx(__uint_as_float(sv[k0 + 1]) - mref);
+              if (i & 1)
+                acc1 = f2_add(acc1, f2_pack(p0, p1));
+              else
+                acc0 = f2_add(acc0, f2_pack(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
           }
         }
-        mt = (c >= 0.f ? fmaxf(e0, e1) : fminf(e0, e1)) * c;
-      } else {
-        // edge tile: scale, mask and keep the scaled values
-        mt = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kBN; ++i) {
-          const float f = (i < lim) ? __uint_as_float(sv[i]) * c : -INFINITY;
-          sv[i] = __float_as_uint(f);
-          mt = fmaxf(mt, f);
+        {
+          float s0, s1;
+          f2_unpack(f2_add(acc0, acc1), s0, s1);
+          l += s0 + s1;
         }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(p_full(t));
       }
-      const float m_new = fmaxf(m, mt);
-      const bool need = m_new > m + kRescaleThreshold;
-      float alpha = 1.f;
-      if (need) {
-        alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-        l *= alpha;
-        m = m_new;
-      }
-      if (__any_sync(0xffffffffu, need && j > 0)) {
-        // move O_t to the new reference maximum (the previous PV has completed:
-        // this tile's S was committed after it)
-#pragma unroll
-        for (int cc = 0; cc < D; cc += 32) {
-          uint32_t o[32];
-          tmem_ld_32x32b_x32(tO + cc, o);
-          tmem_ld_wait_x32(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st_32x32b_x32(tO + cc, o);
-        }
-      }
-      const float mref = (m == -INFINITY) ? 0.f : m;
-      float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int k0 = q * 32 + 2 * i;
-          float p0, p1;
-          if (full_tile) {
-            p0 = ex2_approx(fmaf(__uint_as_float(sv[k0]), c, -mref));
-            p1 = ex2_approx(fmaf(__uint_as_float(sv[k0 + 1]), c, -mref));
-          } else {
-            p0 = ex2_approx(__uint_as_float(sv[k0]) - mref);
-            p1 = ex2_approx(__uint_as_float(sv[k0 + 1]) - mref);
-          }
-          ls0 += p0;
-          ls1 += p1;
-          pk[i] = pack_bf16x2(p0, p1);
-        }
-        tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
-      }
-      l += ls0 + ls1;
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(p_full(t));
-    }
 
-    // ------------------------------------------------------------ epilogue
-    bool have_o = (n_tiles > 0) && !aborted;
-    if (have_o) {
-      const bool ok = mbar_wait(o_done(t), (n_tiles - 1) & 1, abort_flag, to);
-      have_o = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-    }
-    const float inv_l = (l > 0.f && have_o) ? 1.f / l : 0.f;
-    __nv_bfloat16* orow = p.out + ((size_t(b) * p.Sq + token) * p.Hq + (size_t(kvh) * p.G + g)) * D;
-#pragma unroll
-    for (int cc = 0; cc < D; cc += 32) {
-      uint32_t o[32];
+      // ---------------------------------------------------------- epilogue
+      bool have_o = (U.n_tiles > 0) && !aborted;
       if (have_o) {
-        tmem_ld_32x32b_x32(tO + cc, o);
-        tmem_ld_wait_x32(o);
+        const bool ok = mbar_wait(o_done(t), qn & 1, abort_flag, to);
+        have_o = __all_sync(0xffffffffu, ok);
+        if (!have_o) aborted = true;
+        tc_fence_after();
+      }
+      uint32_t o[D];
+      if (have_o) {
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) tmem_ld_32x32b_x32(tO + cc, o + cc);
+        if constexpr (D == 128)
+          tmem_ld_wait_x128(o);
+        else
+          tmem_ld_wait_x32(o), tmem_ld_wait_x32(o + 32);
+        // O_t has been read: the next unit's first PV may overwrite it
+        tc_fence_before();
+        mbar_arrive(o_free(t));
       } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] = 0u;
+        for (int i = 0; i < D; ++i) o[i] = 0u;
       }
-      uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
+      const float inv_l = (l > 0.f && have_o) ? 1.f / l : 0.f;
       if (row_ok) {
-        uint4* dst = reinterpret_cast<uint4*>(orow + cc);
+        __nv_bfloat16* orow = p.out + ((size_t(U.b) * p.Sq + token) * p.Hq + (size_t(U.kvh) * p.G + g)) * D;
+        uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-        for (int v4 = 0; v4 < 4; ++v4)
-          dst[v4] = make_uint4(pk[4 * v4], pk[4 * v4 + 1], pk[4 * v4 + 2], pk[4 * v4 + 3]);
+        for (int v4 = 0; v4 < D / 8; ++v4) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[e] = pack_bf16x2(__uint_as_float(o[8 * v4 + 2 * e]) * inv_l,
+                               __uint_as_float(o[8 * v4 + 2 * e + 1]) * inv_l);
+          dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        if (p.lse) {
+          const float lse = (l > 0.f && have_o) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+          p.lse[(size_t(U.b) * p.Hq + size_t(U.kvh) * p.G + g) * p.Sq + token] = lse;
+        }
       }
-    }
-    if (row_ok && p.lse) {
-      const float lse = (l > 0.f && have_o) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
-      p.lse[(size_t(b) * p.Hq + size_t(kvh) * p.G + g) * p.Sq + token] = lse;
+      if (U.n_tiles > 0) {
+        g_tile += U.n_tiles;
+        ++qn;
+      }
     }
   }
 
