@@ -94,14 +94,14 @@ bool prefill_smem_attr_set(int dev) {
   namespace pf = gqa::prefill;
   static bool done[kMaxDevices] = {false};
   if (dev >= 0 && dev < kMaxDevices && done[dev]) return true;
+  const void* fn = reinterpret_cast<const void*>(pf::prefill_kernel<D>);
+  const int smem = int(pf::Layout<D>::kSmemAlloc);
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, pf::prefill_kernel<D>) != cudaSuccess) return false;
+  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return false;
   static_assert(2 * 128 * pf::kSoftmaxRegs + 128 * pf::kOtherRegs <= pf::kThreads * pf::kLaunchRegs,
                 "register split exceeds the launch budget");
   if (fa.numRegs != pf::kLaunchRegs) return false;
-  if (cudaFuncSetAttribute(pf::prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           int(pf::Layout<D>::kSmemAlloc)) != cudaSuccess)
-    return false;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
   if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
   return true;
 }
@@ -118,9 +118,9 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   // persistent grid: one CTA per SM (the kernel's shared memory and register
   // use allow no more), each looping over work units
   const long long grid = std::min<long long>(n_units, num_sms(current_device()));
-  CUtensorMap tmQ, tmK, tmV;
+  CUtensorMap tmQ, tmK, tmV, tmO;
   if (!encode_4d_bf16(&tmQ, q, D, Hq, Sq, B, 64, G, Mq, 1) || !encode_4d_bf16(&tmK, k, D, Hkv, Sk, B, 64, 1, 128, 1) ||
-      !encode_4d_bf16(&tmV, v, D, Hkv, Sk, B, 64, 1, 128, 1))
+      !encode_4d_bf16(&tmV, v, D, Hkv, Sk, B, 64, 1, 128, 1) || !encode_4d_bf16(&tmO, out, D, Hq, Sq, B, 64, G, Mq, 1))
     return GQA_ERR_CUDA;
   if (!prefill_smem_attr_set<D>(current_device())) return GQA_ERR_CUDA;
   pf::Params p;
@@ -139,7 +139,8 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.timeout_ns = wait_timeout_ns();
-  pf::prefill_kernel<D><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(tmQ, tmK, tmV, p);
+  pf::prefill_kernel<D><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(tmQ, tmK, tmV, tmO,
+                                                                                          p);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 

@@ -26,14 +26,18 @@
 //              read from TMEM (P overwrites S_t as packed bf16)
 //   warps 10-11 idle (they complete the third warpgroup, which hands its
 //              registers to the softmax warpgroups with setmaxnreg)
-// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D).
+// TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D),
+// and with D = 64 the unit's Q tiles Q0 [384,416) Q1 [416,448) as bf16 pairs.
 // The two softmax warpgroups ping-pong: while one computes exponentials the
 // tensor core runs the other's PV and next QK^T.  Across units, the MMA warp
 // starts the next unit's QK^T while the softmax warps are still writing the
 // previous unit's output (S and O are separate TMEM regions); only the first
 // PV of a unit waits for the previous epilogue to have read O_t.  With D = 64
-// the Q tiles are double-buffered so the next unit's Q lands during the
-// current one.
+// QK^T takes Q from TMEM: a tensor-core MMA can read about 64 bytes of shared
+// memory per clock, which two shared-memory operands of a 128x128x16 step
+// exceed by a factor of two, while an operand in TMEM does not count against
+// it; the copy also frees the Q buffer at the start of each unit, so the next
+// unit's Q lands during the current one.
 //
 // Softmax details: t = s * scale * log2(e); the running max m is only moved
 // when a tile's max exceeds it by more than 8 (log2 units); otherwise the
@@ -61,18 +65,25 @@ constexpr float kRescaleThreshold = 8.0f;
 template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;                    // 64-column (128-byte) halves of a row
-  static constexpr int kStages = (D == 64) ? 3 : 2;         // depth of the K ring and of the V ring
-  static constexpr int kQBufs = (D == 64) ? 2 : 1;          // Q tile sets in flight
+  static constexpr int kStages = (D == 64) ? 4 : 2;         // depth of the K ring and of the V ring
+  static constexpr int kQBufs = 1;                          // Q tile sets in shared memory
+  // D = 64: the MMA warp copies the unit's Q tiles into TMEM (tcgen05.cp) and
+  // QK^T reads A from there, which leaves the shared-memory operand bandwidth
+  // to K alone; the Q buffer is free again as soon as the copies complete.
+  static constexpr bool kQInTmem = (D == 64);
   static constexpr uint32_t kHalfBytes = 128u * 128u;       // 128 rows x 128 bytes
   static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;
   static constexpr uint32_t kQSetBytes = kNQT * kTileBytes;
   static constexpr uint32_t kOffQ = 0;
   static constexpr uint32_t kOffK = kOffQ + kQBufs * kQSetBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-  static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+  // epilogue staging: one 128-row x 64-column bf16 block (128-byte swizzle,
+  // the layout of the output tensor map's box) per Q tile
+  static constexpr uint32_t kOffOut = kOffV + kStages * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffOut + kNQT * kHalfBytes;
   // barriers: q_full[QB], q_empty[QB], k_full[S], k_empty[S], v_full[S], v_empty[S],
-  //           s_full[2], p_full[2], o_done[2], o_free[2], drain
-  static constexpr int kNumBars = 2 * kQBufs + 4 * kStages + 4 * kNQT + 1;
+  //           s_full[2], p_full[2], o_done[2], o_free[2], drain, stg_free[2], stg_full[2]
+  static constexpr int kNumBars = 2 * kQBufs + 4 * kStages + 4 * kNQT + 1 + 2 * kNQT;
   static constexpr uint32_t kOffTmemSlot = kOffBar + 8u * kNumBars;
   static constexpr uint32_t kOffAbort = kOffTmemSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
@@ -85,6 +96,8 @@ struct Layout {
   static constexpr uint32_t kTmCols = 512;
   static constexpr uint32_t kTmS0 = 0, kTmS1 = 128;
   static constexpr uint32_t kTmO0 = 256, kTmO1 = 256 + D;
+  static constexpr uint32_t kTmQ0 = 256 + 2 * D, kTmQ1 = 256 + 2 * D + D / 2;   // D = 64 only: bf16 pairs
+  static_assert(!kQInTmem || kTmQ1 + D / 2 <= kTmCols, "TMEM column map overflows");
 };
 
 struct Params {
@@ -105,8 +118,20 @@ struct Unit {
   bool bad_len;
 };
 
-// Work unit u -> (b, kvh, first token, key length, number of key tiles).
-DEVI Unit unit_info(const Params& p, int u) {
+// Key length of work unit u's batch entry.  The load is volatile so that it
+// is issued where it is written (one unit ahead of its use) instead of being
+// moved next to its first use, which would expose its latency.
+DEVI int unit_len(const Params& p, int u) {
+  if (!p.seqlens) return p.Sk;
+  const int b = (u % (p.B * p.Hkv)) / p.Hkv;
+  int v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p.seqlens + b));
+  return v;
+}
+
+// Work unit u -> (b, kvh, first token, key length, number of key tiles);
+// len is unit_len(p, u).
+DEVI Unit unit_info(const Params& p, int u, int len) {
   Unit U;
   const int bh_count = p.B * p.Hkv;
   int qblk = u / bh_count;
@@ -115,7 +140,7 @@ DEVI Unit unit_info(const Params& p, int u) {
   U.b = bh / p.Hkv;
   U.kvh = bh % p.Hkv;
   U.q0 = qblk * kNQT * p.Mq;
-  int Lb = p.seqlens ? __ldg(p.seqlens + U.b) : p.Sk;
+  int Lb = len;
   U.bad_len = (Lb < 0 || Lb > p.Sk);
   if (U.bad_len) Lb = 0;
   U.Lb = Lb;
@@ -129,7 +154,8 @@ DEVI Unit unit_info(const Params& p, int u) {
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const Params p) {
   using L = Layout<D>;
   constexpr int S = L::kStages;
   constexpr int QB = L::kQBufs;
@@ -153,6 +179,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto o_done = [&](int t) { return bar(2 * QB + 4 * S + 2 * kNQT + t); };
   auto o_free = [&](int t) { return bar(2 * QB + 4 * S + 3 * kNQT + t); };
   const uint32_t drain = bar(2 * QB + 4 * S + 4 * kNQT);
+  auto stg_free = [&](int t) { return bar(2 * QB + 4 * S + 4 * kNQT + 1 + t); };
+  auto stg_full = [&](int t) { return bar(2 * QB + 4 * S + 5 * kNQT + 1 + t); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffTmemSlot);
   const uint64_t to = p.timeout_ns;
@@ -173,6 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(p_full(t), 128);
       mbar_init(o_done(t), 1);
       mbar_init(o_free(t), 128);
+      mbar_init(stg_free(t), 1);
+      mbar_init(stg_full(t), 128);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -187,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
   }
   tc_fence_before();
   __syncthreads();
@@ -203,8 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       bool k_only = false;
       const uint32_t q_bytes = uint32_t(kNQT * L::kHalves * 64 * 2 * rows_per_tile);
+      int len_n = unit_len(p, blockIdx.x);     // the grid never exceeds the unit count
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        const Unit U = unit_info(p, u);
+        const Unit U = unit_info(p, u, len_n);
+        // load the next unit's key length now, well before it is needed
+        if (u + int(gridDim.x) < p.n_units) len_n = unit_len(p, u + int(gridDim.x));
         if (U.bad_len) raise_error(kErrBounds);
         if (U.n_tiles == 0) continue;
         const int qb = int(qn % QB);
@@ -263,8 +297,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t off = uint32_t(ks / 4) * L::kHalfBytes + uint32_t(ks % 4) * 32u;
-          umma_ss(dst, make_sdesc_sw128(qa + off, 16, 1024), make_sdesc_sw128(ka + off, 16, 1024),
-                  idesc_s, ks > 0 ? 1u : 0u);
+          if constexpr (L::kQInTmem)
+            umma_ts(dst, tmem + (t ? L::kTmQ1 : L::kTmQ0) + uint32_t(ks) * 8u, make_sdesc_sw128(ka + off, 16, 1024),
+                    idesc_s, ks > 0 ? 1u : 0u);
+          else
+            umma_ss(dst, make_sdesc_sw128(qa + off, 16, 1024), make_sdesc_sw128(ka + off, 16, 1024),
+                    idesc_s, ks > 0 ? 1u : 0u);
+        }
+      };
+      // D = 64: the unit's Q tiles from shared memory into TMEM (executes
+      // after every MMA issued before it, so the previous unit's QK^T are done)
+      auto copy_q = [&](int qb) {
+#pragma unroll
+        for (int t = 0; t < kNQT; ++t) {
+          const uint32_t qa = base + L::kOffQ + qb * L::kQSetBytes + t * L::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            tmem_cp_128x256b(tmem + (t ? L::kTmQ1 : L::kTmQ0) + uint32_t(ks) * 8u,
+                             make_sdesc_sw128(qa + uint32_t(ks) * 32u, 16, 1024));
         }
       };
       auto issue_pv = [&](int t, int s, bool acc) {
@@ -281,8 +331,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g_tile = 0;      // key tiles of earlier units (s_full / p_full phases)
       uint32_t qn = 0;          // units with work so far
       bool ok = true;
+      int len_n = unit_len(p, blockIdx.x);     // the grid never exceeds the unit count
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        const Unit U = unit_info(p, u);
+        const Unit U = unit_info(p, u, len_n);
+        // load the next unit's key length now, well before it is needed
+        if (u + int(gridDim.x) < p.n_units) len_n = unit_len(p, u + int(gridDim.x));
         if (U.n_tiles == 0) continue;
         const int qb = int(qn % QB);
         const int s0 = int(kv_it % S);
@@ -290,12 +343,16 @@ __global__ void __launch_bounds__(kThreads, 1)
              mbar_wait(k_full(s0), (kv_it / S) & 1, abort_flag, to);
         if (!ok) break;
         tc_fence_after();
+        if constexpr (L::kQInTmem) {
+          copy_q(qb);
+          umma_commit(q_empty(qb));     // the Q buffer is free once the copies land
+        }
         for (int t = 0; t < kNQT; ++t) {
           issue_s(t, qb, s0);
           umma_commit(s_full(t));
         }
         umma_commit(k_empty(s0));
-        if (U.n_tiles == 1) umma_commit(q_empty(qb));
+        if (!L::kQInTmem && U.n_tiles == 1) umma_commit(q_empty(qb));
         for (int j = 0; ok && j < U.n_tiles; ++j) {
           const uint32_t it = kv_it + j;
           const int s = int(it % S);
@@ -321,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           umma_commit(v_empty(s));
           if (has_next) umma_commit(k_empty(ns));
-          if (j + 2 == U.n_tiles) umma_commit(q_empty(qb));   // the unit's last QK^T is issued
+          if (!L::kQInTmem && j + 2 == U.n_tiles) umma_commit(q_empty(qb));   // the unit's last QK^T is issued
         }
         kv_it += U.n_tiles;
         g_tile += U.n_tiles;
@@ -349,10 +406,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t c2 = f2_pack(c, c);
     uint32_t g_tile = 0;
     uint32_t qn = 0;
+    uint32_t n_stage = 0;     // uses of this tile's staging block so far
     bool aborted = false;
 
+    int len_n = unit_len(p, blockIdx.x);
     for (int u = blockIdx.x; !aborted && u < p.n_units; u += gridDim.x) {
-      const Unit U = unit_info(p, u);
+      const Unit U = unit_info(p, u, len_n);
+      if (u + int(gridDim.x) < p.n_units) len_n = unit_len(p, u + int(gridDim.x));
       const int token = U.q0 + t * p.Mq + r / p.G;
       const bool row_ok = (r < rows_per_tile) && (token < p.Sq);
       int limit = 0;
@@ -380,101 +440,141 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         const int lim = limit - j * kBN;
         // every key of the tile admissible for every row of the warp and a
-        // positive scale: take the max of the raw scores and fold the scale
-        // into the exponent's FMA.  The choice is warp-uniform because both
-        // branches end in tcgen05.st, which the whole warp must execute together.
+        // positive scale: the max can be taken on the raw scores and the scale
+        // folded into the exponent's FMA.  Every branch below is warp-uniform
+        // because each ends in tcgen05.st, which the whole warp executes together.
         const bool fast = __all_sync(0xffffffffu, lim >= kBN) && (c > 0.f);
-        float mt;
-        if (fast) {
-          float a0 = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
-          float a1 = fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
-          float a2 = fmax3(__uint_as_float(sv[6]), __uint_as_float(sv[7]), __uint_as_float(sv[8]));
-          float a3 = fmax3(__uint_as_float(sv[9]), __uint_as_float(sv[10]), __uint_as_float(sv[11]));
-#pragma unroll
-          for (int i = 12; i < 124; i += 8) {
-            a0 = fmax3(a0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
-            a1 = fmax3(a1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
-            a2 = fmax3(a2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
-            a3 = fmax3(a3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
-          }
-          a0 = fmax3(a0, __uint_as_float(sv[124]), __uint_as_float(sv[125]));
-          a1 = fmax3(a1, __uint_as_float(sv[126]), __uint_as_float(sv[127]));
-          mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c;
-        } else {
-          // edge tile (or non-positive scale): scale, mask, keep the scaled values
-          mt = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < kBN; ++i) {
-            const float f = (i < lim) ? __uint_as_float(sv[i]) * c : -INFINITY;
-            sv[i] = __float_as_uint(f);
-            mt = fmaxf(mt, f);
-          }
-        }
-        const float m_new = fmaxf(m, mt);
-        const bool need = m_new > m + kRescaleThreshold;
-        float alpha = 1.f;
-        if (need) {
-          alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-          l *= alpha;
-          m = m_new;
-        }
-        if (__any_sync(0xffffffffu, need && j > 0)) {
-          // move O_t to the new reference maximum.  The previous PV has
-          // completed: this tile's S was committed after it.
-#pragma unroll
-          for (int cc = 0; cc < D; cc += 32) {
-            uint32_t o[32];
-            tmem_ld_32x32b_x32(tO + cc, o);
-            tmem_ld_wait_x32(o);
-            const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              const uint64_t v = f2_fma(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), a2, 0ull);
-              float lo, hi;
-              f2_unpack(v, lo, hi);
-              o[i] = __float_as_uint(lo);
-              o[i + 1] = __float_as_uint(hi);
-            }
-            tmem_st_32x32b_x32(tO + cc, o);
-          }
-        }
-        const float mref = (m == -INFINITY) ? 0.f : m;
-        uint64_t acc0 = 0ull, acc1 = 0ull;       // packed (+0.0f, +0.0f)
-        if (fast) {
-          const uint64_t nm2 = f2_pack(-mref, -mref);
+        uint64_t acc0 = 0ull, acc1 = 0ull;       // packed (+0.0f, +0.0f) row sums
+        bool done = false;
+        if (fast && __all_sync(0xffffffffu, m != -INFINITY)) {
+          // One pass: exponents against the current reference max m while the
+          // tile max is taken alongside.  Valid when the tile max does not pass
+          // m + threshold (p stays below 2^threshold), which is checked after.
+          const uint64_t nm2 = f2_pack(-m, -m);
+          float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t pk[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int k0 = q * 32 + 2 * i;
+              const float s0 = __uint_as_float(sv[k0]), s1 = __uint_as_float(sv[k0 + 1]);
               float x0, x1;
-              f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), c2, nm2), x0, x1);
+              f2_unpack(f2_fma(f2_pack(s0, s1), c2, nm2), x0, x1);
               const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
               if (i & 1)
                 acc1 = f2_add(acc1, f2_pack(p0, p1));
               else
                 acc0 = f2_add(acc0, f2_pack(p0, p1));
               pk[i] = pack_bf16x2(p0, p1);
+              switch (i & 3) {
+                case 0: a0 = fmax3(a0, s0, s1); break;
+                case 1: a1 = fmax3(a1, s0, s1); break;
+                case 2: a2 = fmax3(a2, s0, s1); break;
+                default: a3 = fmax3(a3, s0, s1); break;
+              }
             }
             tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
           }
-        } else {
+          const float mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c;
+          done = !__any_sync(0xffffffffu, mt > m + kRescaleThreshold);
+        }
+        if (!done) {
+          // Two passes: the tile max first (edge tiles, a row's first tile, or
+          // a max that moved past the threshold), then the exponents.
+          acc0 = 0ull;
+          acc1 = 0ull;
+          float mt;
+          if (fast) {
+            float a0 = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
+            float a1 = fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
+            float a2 = fmax3(__uint_as_float(sv[6]), __uint_as_float(sv[7]), __uint_as_float(sv[8]));
+            float a3 = fmax3(__uint_as_float(sv[9]), __uint_as_float(sv[10]), __uint_as_float(sv[11]));
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int k0 = q * 32 + 2 * i;
-              const float p0 = ex2_approx(__uint_as_float(sv[k0]) - mref);
-              const float p1 = ex2_approx(__uint_as_float(sv[k0 + 1]) - mref);
-              if (i & 1)
-                acc1 = f2_add(acc1, f2_pack(p0, p1));
-              else
-                acc0 = f2_add(acc0, f2_pack(p0, p1));
-              pk[i] = pack_bf16x2(p0, p1);
+            for (int i = 12; i < 124; i += 8) {
+              a0 = fmax3(a0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+              a1 = fmax3(a1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
+              a2 = fmax3(a2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
+              a3 = fmax3(a3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
             }
-            tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
+            a0 = fmax3(a0, __uint_as_float(sv[124]), __uint_as_float(sv[125]));
+            a1 = fmax3(a1, __uint_as_float(sv[126]), __uint_as_float(sv[127]));
+            mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c;
+          } else {
+            // edge tile (or non-positive scale): scale, mask, keep the scaled values
+            mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < kBN; ++i) {
+              const float f = (i < lim) ? __uint_as_float(sv[i]) * c : -INFINITY;
+              sv[i] = __float_as_uint(f);
+              mt = fmaxf(mt, f);
+            }
+          }
+          const float m_new = fmaxf(m, mt);
+          const bool need = m_new > m + kRescaleThreshold;
+          float alpha = 1.f;
+          if (need) {
+            alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+            l *= alpha;
+            m = m_new;
+          }
+          if (__any_sync(0xffffffffu, need && j > 0)) {
+            // move O_t to the new reference maximum.  The previous PV has
+            // completed: this tile's S was committed after it.
+#pragma unroll
+            for (int cc = 0; cc < D; cc += 32) {
+              uint32_t o[32];
+              tmem_ld_32x32b_x32(tO + cc, o);
+              tmem_ld_wait_x32(o);
+              const uint64_t al2 = f2_pack(alpha, alpha);
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                const uint64_t v = f2_fma(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), al2, 0ull);
+                float lo, hi;
+                f2_unpack(v, lo, hi);
+                o[i] = __float_as_uint(lo);
+                o[i + 1] = __float_as_uint(hi);
+              }
+              tmem_st_32x32b_x32(tO + cc, o);
+            }
+          }
+          const float mref = (m == -INFINITY) ? 0.f : m;
+          if (fast) {
+            const uint64_t nm2 = f2_pack(-mref, -mref);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int k0 = q * 32 + 2 * i;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), c2, nm2), x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                if (i & 1)
+                  acc1 = f2_add(acc1, f2_pack(p0, p1));
+                else
+                  acc0 = f2_add(acc0, f2_pack(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+              tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
+            }
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int k0 = q * 32 + 2 * i;
+                const float p0 = ex2_approx(__uint_as_float(sv[k0]) - mref);
+                const float p1 = ex2_approx(__uint_as_float(sv[k0 + 1]) - mref);
+                if (i & 1)
+                  acc1 = f2_add(acc1, f2_pack(p0, p1));
+                else
+                  acc0 = f2_add(acc0, f2_pack(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+              tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
+            }
           }
         }
         {
@@ -511,19 +611,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < D; ++i) o[i] = 0u;
       }
       const float inv_l = (l > 0.f && have_o) ? 1.f / l : 0.f;
-      if (row_ok) {
-        __nv_bfloat16* orow = p.out + ((size_t(U.b) * p.Sq + token) * p.Hq + (size_t(U.kvh) * p.G + g)) * D;
-        uint4* dst = reinterpret_cast<uint4*>(orow);
+      if (!aborted) {
+        // Normalised bf16 rows go to a staging block in shared memory, 64
+        // columns at a time, and one thread writes each block to global memory
+        // with a TMA store (rows of tokens past Sq fall outside the tensor and
+        // are not written).  Row r of the block is 128 bytes; its 16-byte chunk
+        // c sits at position c ^ (r % 8), the 128-byte swizzle of the map.  The
+        // hand-offs use mbarriers with bounded waits (not bar.sync), so a warp
+        // that gave up on an earlier wait cannot leave the others blocked.
+        const uint32_t stage = base + L::kOffOut + uint32_t(t) * L::kHalfBytes;
+        const bool leader = (wq == 0 && lane == 0);
 #pragma unroll
-        for (int v4 = 0; v4 < D / 8; ++v4) {
-          uint32_t w[4];
+        for (int h = 0; h < L::kHalves; ++h) {
+          const uint32_t ph = n_stage & 1;
+          ++n_stage;
+          if (leader) {
+            bulk_wait_read_all();        // the previous store has finished reading the block
+            mbar_arrive(stg_free(t));
+          }
+          bool ok = mbar_wait(stg_free(t), ph, abort_flag, to);
+          if (ok) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            w[e] = pack_bf16x2(__uint_as_float(o[8 * v4 + 2 * e]) * inv_l,
-                               __uint_as_float(o[8 * v4 + 2 * e + 1]) * inv_l);
-          dst[v4] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int c8 = 0; c8 < 8; ++c8) {
+              uint32_t w[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int col = h * 64 + c8 * 8 + 2 * e;
+                w[e] = pack_bf16x2(__uint_as_float(o[col]) * inv_l, __uint_as_float(o[col + 1]) * inv_l);
+              }
+              const uint32_t addr = stage + uint32_t(r) * 128u + (uint32_t(c8 ^ (r & 7)) << 4);
+              asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                           "r"(w[2]), "r"(w[3])
+                           : "memory");
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(stg_full(t));
+          }
+          if (leader && ok && mbar_wait(stg_full(t), ph, abort_flag, to)) {
+            tma_store_4d(&tmO, stage, h * 64, U.kvh * p.G, U.q0 + t * p.Mq, U.b);
+            bulk_commit_group();
+          }
         }
-        if (p.lse) {
+        if (row_ok && p.lse) {
           const float lse = (l > 0.f && have_o) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
           p.lse[(size_t(U.b) * p.Hq + size_t(U.kvh) * p.G + g) * p.Sq + token] = lse;
         }
@@ -535,6 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  if (warp < 8 && (warp & 3) == 0 && lane == 0) bulk_wait_all();   // the epilogue's TMA stores
   tc_fence_before();
   __syncthreads();
   if (warp == kWarpMMA) {

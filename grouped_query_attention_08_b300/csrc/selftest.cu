@@ -1,7 +1,8 @@
 // selftest.cu -- libgqa_selftest: single-CTA checks of the sm_103a building
 // blocks the prefill kernel is made of, for the GPU test suite only:
 //   gqa_selftest_qk  S = A . B^T  (TMA 128B-swizzled loads, K-major smem
-//                    descriptors, tcgen05.mma kind::f16, tcgen05.ld)
+//                    descriptors, tcgen05.mma kind::f16, tcgen05.ld; optionally
+//                    A copied into TMEM with tcgen05.cp and read from there)
 //   gqa_selftest_pv  O = P . V    (P packed to bf16 and stored to TMEM with
 //                    tcgen05.st, used as the A operand from TMEM; V MN-major
 //                    in 128B-swizzled smem, N = 64 or 128)
@@ -19,9 +20,11 @@ using namespace gqa;
 
 constexpr uint32_t kHalf = 128u * 128u;   // 128 rows x 128 bytes
 
-// S[128][128] = A[128][64] . B[128][64]^T
+// S[128][128] = A[128][64] . B[128][64]^T.  use_cp: A is first copied from
+// shared memory into TMEM with tcgen05.cp and read by the MMA from there.
 __global__ void __launch_bounds__(128, 1)
-    qk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, float* S) {
+    qk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, float* S,
+              int use_cp) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -37,7 +40,7 @@ __global__ void __launch_bounds__(128, 1)
     fence_proxy_async_smem();
   }
   if (warp == 0) {
-    tmem_alloc(smem_u32(slot), 128);
+    tmem_alloc(smem_u32(slot), 256);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -52,9 +55,15 @@ __global__ void __launch_bounds__(128, 1)
     mbar_wait(bar_ld, 0, &no_abort, 1000000000ull);
     tc_fence_after();
     const uint32_t idesc = make_idesc_bf16(128, 128, 0, 0);
-    for (int ks = 0; ks < 4; ++ks)
-      umma_ss(tmem, make_sdesc_sw128(a_s + ks * 32, 16, 1024), make_sdesc_sw128(b_s + ks * 32, 16, 1024), idesc,
-              ks > 0);
+    if (use_cp) {
+      for (int ks = 0; ks < 4; ++ks) tmem_cp_128x256b(tmem + 128 + ks * 8, make_sdesc_sw128(a_s + ks * 32, 16, 1024));
+      for (int ks = 0; ks < 4; ++ks)
+        umma_ts(tmem, tmem + 128 + ks * 8, make_sdesc_sw128(b_s + ks * 32, 16, 1024), idesc, ks > 0);
+    } else {
+      for (int ks = 0; ks < 4; ++ks)
+        umma_ss(tmem, make_sdesc_sw128(a_s + ks * 32, 16, 1024), make_sdesc_sw128(b_s + ks * 32, 16, 1024), idesc,
+                ks > 0);
+    }
     umma_commit(bar_mma);
   }
   __syncwarp();
@@ -72,7 +81,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -170,13 +179,14 @@ bool map_2d(CUtensorMap* m, const void* p, int rows, int cols) {
 
 extern "C" {
 
-// A, B: device bf16 [128][64]; S: device fp32 [128][128].  Synchronous.
-int gqa_selftest_qk(const void* A, const void* B, float* S) {
+// A, B: device bf16 [128][64]; S: device fp32 [128][128].  use_cp: A reaches
+// the MMA through TMEM (tcgen05.cp) instead of shared memory.  Synchronous.
+int gqa_selftest_qk(const void* A, const void* B, float* S, int use_cp) {
   CUtensorMap ma, mb;
   if (!map_2d(&ma, A, 128, 64) || !map_2d(&mb, B, 128, 64)) return 3;
   const int smem = 4 * kHalf + 1024 + 64;
   if (cudaFuncSetAttribute(qk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return 3;
-  qk_kernel<<<1, 128, smem>>>(ma, mb, S);
+  qk_kernel<<<1, 128, smem>>>(ma, mb, S, use_cp ? 1 : 0);
   return cudaDeviceSynchronize() == cudaSuccess ? 0 : 3;
 }
 

@@ -16,19 +16,20 @@ def st():
     build.build()
     lib = ctypes.CDLL(build.lib_path("libgqa_selftest.so"))
     lib.gqa_selftest_qk.restype = ctypes.c_int
-    lib.gqa_selftest_qk.argtypes = [ctypes.c_void_p] * 3
+    lib.gqa_selftest_qk.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int]
     lib.gqa_selftest_pv.restype = ctypes.c_int
     lib.gqa_selftest_pv.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int, ctypes.c_uint, ctypes.c_uint]
     return lib
 
 
-def test_tma_swizzle_and_kmajor_mma(st):
-    g = torch.Generator().manual_seed(0)
+@pytest.mark.parametrize("use_cp", [0, 1], ids=["a_from_smem", "a_copied_to_tmem"])
+def test_tma_swizzle_and_kmajor_mma(st, use_cp):
+    g = torch.Generator().manual_seed(use_cp)
     A = torch.randn(128, 64, generator=g).to(torch.bfloat16)
     B = torch.randn(128, 64, generator=g).to(torch.bfloat16)
     S = torch.zeros(128, 128, device="cuda")
     dA, dB = A.cuda(), B.cuda()          # keep the device copies alive across the call
-    rc = st.gqa_selftest_qk(dA.data_ptr(), dB.data_ptr(), S.data_ptr())
+    rc = st.gqa_selftest_qk(dA.data_ptr(), dB.data_ptr(), S.data_ptr(), use_cp)
     assert rc == 0
     ref = A.double() @ B.double().T
     err = (S.cpu().double() - ref).abs().max().item()
