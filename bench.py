@@ -248,6 +248,36 @@ def run_reference(args):
     return 0
 
 
+def time_prefill_workload(gqa, name, device, flush, reps=10, warmup=3):
+    """Per-call time of gqa_fwd on a named prefill workload (CUDA events, L2
+    flushed before every call); returns TFLOP/s of algorithmic work."""
+    w = inputs.WORKLOADS[name]
+    inp = inputs.make_workload(w)
+    d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    lens = None if inp["seqlens_k"] is None else inp["seqlens_k"].tolist()
+    flops = roofline.prefill_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal, lens)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=device)
+
+    def call():
+        gqa.gqa_fwd(d["q"], d["k"], d["v"], causal=w.causal, seqlens_k=d["seqlens_k"], scale=w.scale,
+                    out=out, lse=lse)
+
+    for _ in range(warmup):
+        flush.fill_(1)
+        call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record()
+        call()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / reps
+    return {"tflops": flops / (ms * 1e-3) / 1e12, "ms": ms, "workload": _workload_name(w),
+            "algorithmic_flops_per_launch": flops}
+
+
 def _workload_name(w):
     lens = "full" if w.lens is None else "U[%d,%d]" % w.lens
     return "%s prefill B%d Hq%d Hkv%d Sq%d Sk%d D%d %s keys %s" % (
@@ -265,6 +295,9 @@ def main():
     ap.add_argument("--decode", default="llama_decode")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip timing the other prefill workloads after the main run")
+    ap.add_argument("--other-reps", type=int, default=10)
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -402,6 +435,19 @@ def main():
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "what": "prefill through gqa_fwd with pinned host inputs copied in and out every step"}
 
+    # ---- the other prefill workloads, timed the same way (not part of `value`)
+    others = {}
+    if not args.no_other_workloads:
+        del P, pin, out_p, lse_p
+        for name in ("bert_base", "bert_large_long", "causal_long"):
+            if name == args.prefill:
+                others[name] = {"tflops": value / ws, "ms": pre_avg * 1e3}
+                continue
+            others[name] = time_prefill_workload(gqa, name, device, flush, reps=args.other_reps)
+        torch.cuda.synchronize()
+        if gqa.gqa_device_status() != 0:
+            raise RuntimeError("device error while timing the other prefill workloads")
+
     cb = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cb = cpu_baseline(args.prefill)
@@ -425,6 +471,7 @@ def main():
             "e2e": e2e,
             "gpu_launches": launches_per_step * K,
             "cpu_baseline": cb,
+            "prefill_workloads": others,
         }
         print(json.dumps(line))
     if ws > 1:
