@@ -39,11 +39,14 @@
 // it; the copy also frees the Q buffer at the start of each unit, so the next
 // unit's Q lands during the current one.
 //
-// Softmax details: t = s * scale * log2(e); the running max m is only moved
-// when a tile's max exceeds it by more than 8 (log2 units); otherwise the
-// stale m is kept, probabilities are bounded by 2^8 and the final division
-// by l = sum p is exact for any reference m.  Masked keys (j >= L_b, or
-// j > i + Sk - Sq when causal) get p = 0 exactly.
+// Softmax details: t = s * scale * log2(e).  Exponents are taken in one pass
+// against a reference max (the running max; for a row's first tile the max of
+// its first 8 admissible scores), which may be below the true max: the final
+// division by l = sum p is exact for any reference.  The pass is kept when the
+// tile's row sum stays below 2^20 (so no p exceeds it); otherwise the tile is
+// redone against its true max, and the running max moves only when it grows
+// by more than 8 (log2 units).  Masked keys (j >= L_b, or j > i + Sk - Sq when
+// causal) get p = 0 exactly.
 #pragma once
 
 #include "common.cuh"
@@ -61,6 +64,9 @@ constexpr int kSoftmaxRegs = 216;   // 2 x 128 x 216 + 128 x 72 = 384 x 168 regi
 constexpr int kLaunchRegs = 168;
 constexpr int kOtherRegs = 72;
 constexpr float kRescaleThreshold = 8.0f;
+// A one-pass tile is kept while its row sum stays below this (2^20): then no
+// probability exceeds 2^20 and the fp32 accumulators stay far from overflow.
+constexpr float kOnePassSumLimit = 1048576.0f;
 
 template <int D>
 struct Layout {
@@ -439,76 +445,85 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld_wait_x128(sv);
 
         const int lim = limit - j * kBN;
-        // every key of the tile admissible for every row of the warp and a
-        // positive scale: the max can be taken on the raw scores and the scale
-        // folded into the exponent's FMA.  Every branch below is warp-uniform
-        // because each ends in tcgen05.st, which the whole warp executes together.
+        // Every key of the tile admissible for every row of the warp and a
+        // positive scale: no mask is needed and the max can be taken on the
+        // raw scores.  Every branch below is warp-uniform because each ends in
+        // tcgen05.st, which the whole warp executes together.
         const bool fast = __all_sync(0xffffffffu, lim >= kBN) && (c > 0.f);
         uint64_t acc0 = 0ull, acc1 = 0ull;       // packed (+0.0f, +0.0f) row sums
         bool done = false;
-        if (fast && __all_sync(0xffffffffu, m != -INFINITY)) {
-          // One pass: exponents against the current reference max m while the
-          // tile max is taken alongside.  Valid when the tile max does not pass
-          // m + threshold (p stays below 2^threshold), which is checked after.
-          const uint64_t nm2 = f2_pack(-m, -m);
-          float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+        if (c > 0.f) {
+          // One pass against a reference max: the running max m, or for a
+          // row's first tile the max of its first 8 admissible scores.  The
+          // reference may sit below the true max; that is exact after the
+          // final division as long as no p grows large, so the pass is kept
+          // when the tile's row sum stays below kOnePassSumLimit (no p can
+          // exceed it) and is redone against the true max otherwise.
+          float mref = m;
+          if (m == -INFINITY) {
+            float m8 = -INFINITY;
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int k0 = q * 32 + 2 * i;
-              const float s0 = __uint_as_float(sv[k0]), s1 = __uint_as_float(sv[k0 + 1]);
-              float x0, x1;
-              f2_unpack(f2_fma(f2_pack(s0, s1), c2, nm2), x0, x1);
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              if (i & 1)
-                acc1 = f2_add(acc1, f2_pack(p0, p1));
-              else
-                acc0 = f2_add(acc0, f2_pack(p0, p1));
-              pk[i] = pack_bf16x2(p0, p1);
-              switch (i & 3) {
-                case 0: a0 = fmax3(a0, s0, s1); break;
-                case 1: a1 = fmax3(a1, s0, s1); break;
-                case 2: a2 = fmax3(a2, s0, s1); break;
-                default: a3 = fmax3(a3, s0, s1); break;
-              }
-            }
-            tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
+            for (int i = 0; i < 8; ++i)
+              if (i < lim) m8 = fmaxf(m8, __uint_as_float(sv[i]));
+            mref = (m8 == -INFINITY) ? 0.f : m8 * c;
           }
-          const float mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c;
-          done = !__any_sync(0xffffffffu, mt > m + kRescaleThreshold);
+          const uint64_t nm2 = f2_pack(-mref, -mref);
+          if (fast) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int k0 = q * 32 + 2 * i;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), c2, nm2), x0, x1);
+                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                if (i & 1)
+                  acc1 = f2_add(acc1, f2_pack(p0, p1));
+                else
+                  acc0 = f2_add(acc0, f2_pack(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+              tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
+            }
+          } else {
+            // edge tile: keys at or past the row's limit get exactly zero weight
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int k0 = q * 32 + 2 * i;
+                float x0, x1;
+                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), c2, nm2), x0, x1);
+                const float p0 = ex2_approx(k0 < lim ? x0 : -INFINITY);
+                const float p1 = ex2_approx(k0 + 1 < lim ? x1 : -INFINITY);
+                if (i & 1)
+                  acc1 = f2_add(acc1, f2_pack(p0, p1));
+                else
+                  acc0 = f2_add(acc0, f2_pack(p0, p1));
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+              tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
+            }
+          }
+          float t0, t1;
+          f2_unpack(f2_add(acc0, acc1), t0, t1);
+          const float tile_sum = t0 + t1;
+          done = !__any_sync(0xffffffffu, !(tile_sum <= kOnePassSumLimit));
+          if (done && m == -INFINITY && tile_sum > 0.f) m = mref;
         }
         if (!done) {
-          // Two passes: the tile max first (edge tiles, a row's first tile, or
-          // a max that moved past the threshold), then the exponents.
+          // Two passes: the tile max first, then the exponents (a non-positive
+          // scale, or a tile whose scores rose far above the reference).
           acc0 = 0ull;
           acc1 = 0ull;
-          float mt;
-          if (fast) {
-            float a0 = fmax3(__uint_as_float(sv[0]), __uint_as_float(sv[1]), __uint_as_float(sv[2]));
-            float a1 = fmax3(__uint_as_float(sv[3]), __uint_as_float(sv[4]), __uint_as_float(sv[5]));
-            float a2 = fmax3(__uint_as_float(sv[6]), __uint_as_float(sv[7]), __uint_as_float(sv[8]));
-            float a3 = fmax3(__uint_as_float(sv[9]), __uint_as_float(sv[10]), __uint_as_float(sv[11]));
+          float mt = -INFINITY;
 #pragma unroll
-            for (int i = 12; i < 124; i += 8) {
-              a0 = fmax3(a0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
-              a1 = fmax3(a1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
-              a2 = fmax3(a2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
-              a3 = fmax3(a3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
-            }
-            a0 = fmax3(a0, __uint_as_float(sv[124]), __uint_as_float(sv[125]));
-            a1 = fmax3(a1, __uint_as_float(sv[126]), __uint_as_float(sv[127]));
-            mt = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3)) * c;
-          } else {
-            // edge tile (or non-positive scale): scale, mask, keep the scaled values
-            mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < kBN; ++i) {
-              const float f = (i < lim) ? __uint_as_float(sv[i]) * c : -INFINITY;
-              sv[i] = __float_as_uint(f);
-              mt = fmaxf(mt, f);
-            }
+          for (int i = 0; i < kBN; ++i) {
+            const float f = (i < lim) ? __uint_as_float(sv[i]) * c : -INFINITY;
+            sv[i] = __float_as_uint(f);
+            mt = fmaxf(mt, f);
           }
           const float m_new = fmaxf(m, mt);
           const bool need = m_new > m + kRescaleThreshold;
@@ -539,42 +554,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const float mref = (m == -INFINITY) ? 0.f : m;
-          if (fast) {
-            const uint64_t nm2 = f2_pack(-mref, -mref);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t pk[16];
+          for (int q = 0; q < 4; ++q) {
+            uint32_t pk[16];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int k0 = q * 32 + 2 * i;
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), c2, nm2), x0, x1);
-                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                if (i & 1)
-                  acc1 = f2_add(acc1, f2_pack(p0, p1));
-                else
-                  acc0 = f2_add(acc0, f2_pack(p0, p1));
-                pk[i] = pack_bf16x2(p0, p1);
-              }
-              tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
+            for (int i = 0; i < 16; ++i) {
+              const int k0 = q * 32 + 2 * i;
+              const float p0 = ex2_approx(__uint_as_float(sv[k0]) - mref);
+              const float p1 = ex2_approx(__uint_as_float(sv[k0 + 1]) - mref);
+              if (i & 1)
+                acc1 = f2_add(acc1, f2_pack(p0, p1));
+              else
+                acc0 = f2_add(acc0, f2_pack(p0, p1));
+              pk[i] = pack_bf16x2(p0, p1);
             }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int k0 = q * 32 + 2 * i;
-                const float p0 = ex2_approx(__uint_as_float(sv[k0]) - mref);
-                const float p1 = ex2_approx(__uint_as_float(sv[k0 + 1]) - mref);
-                if (i & 1)
-                  acc1 = f2_add(acc1, f2_pack(p0, p1));
-                else
-                  acc0 = f2_add(acc0, f2_pack(p0, p1));
-                pk[i] = pack_bf16x2(p0, p1);
-              }
-              tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
-            }
+            tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
           }
         }
         {
