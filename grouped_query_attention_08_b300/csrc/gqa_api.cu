@@ -136,6 +136,13 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   p.Mq = Mq;
   p.n_qblk = int(n_qblk);
   p.n_units = int(n_units);
+  {
+    const long long bh_count = (long long)B * Hkv;
+    p.step_q = int(grid / bh_count);
+    const long long rem = grid % bh_count;
+    p.step_b = int(rem / Hkv);
+    p.step_kvh = int(rem % Hkv);
+  }
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.timeout_ns = wait_timeout_ns();

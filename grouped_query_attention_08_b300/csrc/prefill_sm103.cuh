@@ -114,6 +114,8 @@ struct Params {
   int Mq;                 // tokens per Q tile (G * Mq <= 128)
   int n_qblk;             // ceil(Sq / (kNQT * Mq))
   int n_units;            // n_qblk * B * Hkv
+  // gridDim.x as unit-index steps: gridDim.x = step_q * B * Hkv + step_b * Hkv + step_kvh
+  int step_q, step_b, step_kvh;
   int causal;
   float scale_log2;       // scale * log2(e)
   unsigned long long timeout_ns;
@@ -124,27 +126,56 @@ struct Unit {
   bool bad_len;
 };
 
-// Key length of work unit u's batch entry.  The load is volatile so that it
-// is issued where it is written (one unit ahead of its use) instead of being
+// Position of work unit u = qidx * (B * Hkv) + b * Hkv + kvh.  A CTA walks
+// units c, c + gridDim.x, ...; the position advances by adding the
+// precomputed steps with carries, so the walk needs no integer division.
+struct UnitPos {
+  int u, qidx, b, kvh;
+};
+DEVI UnitPos upos_first(const Params& p) {
+  UnitPos x;
+  x.u = int(blockIdx.x);
+  const int bh_count = p.B * p.Hkv;
+  x.qidx = x.u / bh_count;
+  const int bh = x.u % bh_count;
+  x.b = bh / p.Hkv;
+  x.kvh = bh % p.Hkv;
+  return x;
+}
+DEVI void upos_next(UnitPos& x, const Params& p) {
+  x.u += int(gridDim.x);
+  x.kvh += p.step_kvh;
+  int carry = 0;
+  if (x.kvh >= p.Hkv) {
+    x.kvh -= p.Hkv;
+    carry = 1;
+  }
+  x.b += p.step_b + carry;
+  carry = 0;
+  if (x.b >= p.B) {
+    x.b -= p.B;
+    carry = 1;
+  }
+  x.qidx += p.step_q + carry;
+}
+
+// Key length of the unit's batch entry.  The load is volatile so that it is
+// issued where it is written (one unit ahead of its use) instead of being
 // moved next to its first use, which would expose its latency.
-DEVI int unit_len(const Params& p, int u) {
+DEVI int unit_len(const Params& p, const UnitPos& x) {
   if (!p.seqlens) return p.Sk;
-  const int b = (u % (p.B * p.Hkv)) / p.Hkv;
   int v;
-  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p.seqlens + b));
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p.seqlens + x.b));
   return v;
 }
 
-// Work unit u -> (b, kvh, first token, key length, number of key tiles);
-// len is unit_len(p, u).
-DEVI Unit unit_info(const Params& p, int u, int len) {
+// Work unit -> (b, kvh, first token, key length, number of key tiles); len is
+// unit_len of the same unit.
+DEVI Unit unit_info(const Params& p, const UnitPos& x, int len) {
   Unit U;
-  const int bh_count = p.B * p.Hkv;
-  int qblk = u / bh_count;
-  if (p.causal) qblk = p.n_qblk - 1 - qblk;     // longest units first
-  const int bh = u % bh_count;
-  U.b = bh / p.Hkv;
-  U.kvh = bh % p.Hkv;
+  const int qblk = p.causal ? p.n_qblk - 1 - x.qidx : x.qidx;   // causal: longest units first
+  U.b = x.b;
+  U.kvh = x.kvh;
   U.q0 = qblk * kNQT * p.Mq;
   int Lb = len;
   U.bad_len = (Lb < 0 || Lb > p.Sk);
@@ -240,11 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       bool k_only = false;
       const uint32_t q_bytes = uint32_t(kNQT * L::kHalves * 64 * 2 * rows_per_tile);
-      int len_n = unit_len(p, blockIdx.x);     // the grid never exceeds the unit count
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        const Unit U = unit_info(p, u, len_n);
+      UnitPos xn = upos_first(p);              // the grid never exceeds the unit count
+      int len_n = unit_len(p, xn);
+      for (UnitPos x = xn; ok && x.u < p.n_units; x = xn) {
+        const Unit U = unit_info(p, x, len_n);
         // load the next unit's key length now, well before it is needed
-        if (u + int(gridDim.x) < p.n_units) len_n = unit_len(p, u + int(gridDim.x));
+        upos_next(xn, p);
+        if (xn.u < p.n_units) len_n = unit_len(p, xn);
         if (U.bad_len) raise_error(kErrBounds);
         if (U.n_tiles == 0) continue;
         const int qb = int(qn % QB);
@@ -337,11 +370,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g_tile = 0;      // key tiles of earlier units (s_full / p_full phases)
       uint32_t qn = 0;          // units with work so far
       bool ok = true;
-      int len_n = unit_len(p, blockIdx.x);     // the grid never exceeds the unit count
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        const Unit U = unit_info(p, u, len_n);
+      UnitPos xn = upos_first(p);              // the grid never exceeds the unit count
+      int len_n = unit_len(p, xn);
+      for (UnitPos x = xn; ok && x.u < p.n_units; x = xn) {
+        const Unit U = unit_info(p, x, len_n);
         // load the next unit's key length now, well before it is needed
-        if (u + int(gridDim.x) < p.n_units) len_n = unit_len(p, u + int(gridDim.x));
+        upos_next(xn, p);
+        if (xn.u < p.n_units) len_n = unit_len(p, xn);
         if (U.n_tiles == 0) continue;
         const int qb = int(qn % QB);
         const int s0 = int(kv_it % S);
@@ -415,11 +450,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t n_stage = 0;     // uses of this tile's staging block so far
     bool aborted = false;
 
-    int len_n = unit_len(p, blockIdx.x);
-    for (int u = blockIdx.x; !aborted && u < p.n_units; u += gridDim.x) {
-      const Unit U = unit_info(p, u, len_n);
-      if (u + int(gridDim.x) < p.n_units) len_n = unit_len(p, u + int(gridDim.x));
-      const int token = U.q0 + t * p.Mq + r / p.G;
+    const int r_tok = r / p.G;   // token of this row within the Q tile
+    UnitPos xn = upos_first(p);
+    int len_n = unit_len(p, xn);
+    for (UnitPos x = xn; !aborted && x.u < p.n_units; x = xn) {
+      const Unit U = unit_info(p, x, len_n);
+      upos_next(xn, p);
+      if (xn.u < p.n_units) len_n = unit_len(p, xn);
+      const int token = U.q0 + t * p.Mq + r_tok;
       const bool row_ok = (r < rows_per_tile) && (token < p.Sq);
       int limit = 0;
       if (row_ok) {
@@ -447,9 +485,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = limit - j * kBN;
         // Every key of the tile admissible for every row of the warp and a
         // positive scale: no mask is needed and the max can be taken on the
-        // raw scores.  Every branch below is warp-uniform because each ends in
-        // tcgen05.st, which the whole warp executes together.
-        const bool fast = __all_sync(0xffffffffu, lim >= kBN) && (c > 0.f);
+        // raw scores.  Rows that hold no query (past the tile's G * Mq rows or
+        // past Sq) are never stored, so they neither force the masked path nor
+        // vote for a second pass.  Every branch below is warp-uniform because
+        // each ends in tcgen05.st, which the whole warp executes together.
+        const bool fast = __all_sync(0xffffffffu, lim >= kBN || !row_ok) && (c > 0.f);
         uint64_t acc0 = 0ull, acc1 = 0ull;       // packed (+0.0f, +0.0f) row sums
         bool done = false;
         if (c > 0.f) {
@@ -510,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           float t0, t1;
           f2_unpack(f2_add(acc0, acc1), t0, t1);
           const float tile_sum = t0 + t1;
-          done = !__any_sync(0xffffffffu, !(tile_sum <= kOnePassSumLimit));
+          done = !__any_sync(0xffffffffu, row_ok && !(tile_sum <= kOnePassSumLimit));
           if (done && m == -INFINITY && tile_sum > 0.f) m = mref;
         }
         if (!done) {
