@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include <cuda.h>
@@ -68,6 +69,29 @@ EncodeTiledFn encode_fn() {
       fn = reinterpret_cast<EncodeTiledFn>(p);
   });
   return fn;
+}
+
+// Work-unit scheduler slots of the prefill kernel: each launch takes the next
+// slot (a claim counter and a finished-CTA counter); the launch's last CTA
+// puts the slot back to zero.  Launches that use one slot must not overlap on
+// the GPU, which holds unless kSchedSlots launches are in flight at once.
+constexpr int kSchedSlots = 64;
+__device__ unsigned int g_prefill_sched[2 * kSchedSlots];
+std::atomic<unsigned> g_sched_next{0};
+
+unsigned int* sched_slot(int dev) {
+  static unsigned int* base[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!base[dev]) {
+      void* ptr = nullptr;
+      if (cudaGetSymbolAddress(&ptr, g_prefill_sched) != cudaSuccess) return nullptr;
+      base[dev] = static_cast<unsigned int*>(ptr);
+    }
+  }
+  return base[dev] + 2 * (g_sched_next.fetch_add(1) % kSchedSlots);
 }
 
 // 4-D bf16 tensor map over a row-major [d3][d2][d1][d0] array, 128-byte
@@ -136,13 +160,8 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   p.Mq = Mq;
   p.n_qblk = int(n_qblk);
   p.n_units = int(n_units);
-  {
-    const long long bh_count = (long long)B * Hkv;
-    p.step_q = int(grid / bh_count);
-    const long long rem = grid % bh_count;
-    p.step_b = int(rem / Hkv);
-    p.step_kvh = int(rem % Hkv);
-  }
+  p.sched = sched_slot(current_device());
+  if (!p.sched) return GQA_ERR_CUDA;
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.timeout_ns = wait_timeout_ns();

@@ -17,8 +17,9 @@
 //
 // Work unit: batch b, K/V head kvh, and 2 consecutive Q tiles of Mq =
 // floor(128/G) tokens x G heads each.  The grid is persistent (at most one
-// CTA per SM); CTA c takes units c, c + gridDim.x, ...  Causal launches
-// number the units longest first.  Warp roles (384 threads):
+// CTA per SM); CTA c starts with unit c and then claims units from a counter
+// in global memory (dynamic scheduling evens out units of different length).
+// Causal launches number the units longest first.  Warp roles (384 threads):
 //   warps 0-3  softmax + epilogue for Q tile 0 (thread = one row = one TMEM lane)
 //   warps 4-7  softmax + epilogue for Q tile 1
 //   warp  8    TMA producer: the unit's Q tiles, then a K ring and a V ring
@@ -64,6 +65,9 @@ constexpr int kSoftmaxRegs = 216;   // 2 x 128 x 216 + 128 x 72 = 384 x 168 regi
 constexpr int kLaunchRegs = 168;
 constexpr int kOtherRegs = 72;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr int kUQ = 4;                // depth of the shared-memory work-unit queue
+// consumers of a queue entry: the MMA-issuing thread and every softmax thread
+constexpr uint32_t kUQConsumers = 1 + kNQT * 128;
 // A one-pass tile is kept while its row sum stays below this (2^20): then no
 // probability exceeds 2^20 and the fp32 accumulators stay far from overflow.
 constexpr float kOnePassSumLimit = 1048576.0f;
@@ -88,9 +92,12 @@ struct Layout {
   static constexpr uint32_t kOffOut = kOffV + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffOut + kNQT * kHalfBytes;
   // barriers: q_full[QB], q_empty[QB], k_full[S], k_empty[S], v_full[S], v_empty[S],
-  //           s_full[2], p_full[2], o_done[2], o_free[2], drain, stg_free[2], stg_full[2]
-  static constexpr int kNumBars = 2 * kQBufs + 4 * kStages + 4 * kNQT + 1 + 2 * kNQT;
-  static constexpr uint32_t kOffTmemSlot = kOffBar + 8u * kNumBars;
+  //           s_full[2], p_full[2], o_done[2], o_free[2], drain, stg_free[2], stg_full[2],
+  //           uq_full[kUQ], uq_empty[kUQ]
+  static constexpr int kNumBars = 2 * kQBufs + 4 * kStages + 4 * kNQT + 1 + 2 * kNQT + 2 * kUQ;
+  // unit queue: kUQ entries of (unit index, key length)
+  static constexpr uint32_t kOffUQ = kOffBar + 8u * kNumBars;
+  static constexpr uint32_t kOffTmemSlot = kOffUQ + 8u * kUQ;
   static constexpr uint32_t kOffAbort = kOffTmemSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
   static constexpr uint32_t kSmemAlloc = kBytes + 1024u;    // slack to align the base to 1024 B
@@ -114,8 +121,10 @@ struct Params {
   int Mq;                 // tokens per Q tile (G * Mq <= 128)
   int n_qblk;             // ceil(Sq / (kNQT * Mq))
   int n_units;            // n_qblk * B * Hkv
-  // gridDim.x as unit-index steps: gridDim.x = step_q * B * Hkv + step_b * Hkv + step_kvh
-  int step_q, step_b, step_kvh;
+  // Work-unit scheduler of this launch: sched[0] counts units claimed past
+  // the first gridDim.x, sched[1] counts CTAs that finished; the last CTA to
+  // finish sets both back to zero for the next launch that uses the slot.
+  unsigned int* sched;
   int causal;
   float scale_log2;       // scale * log2(e)
   unsigned long long timeout_ns;
@@ -126,47 +135,36 @@ struct Unit {
   bool bad_len;
 };
 
-// Position of work unit u = qidx * (B * Hkv) + b * Hkv + kvh.  A CTA walks
-// units c, c + gridDim.x, ...; the position advances by adding the
-// precomputed steps with carries, so the walk needs no integer division.
+// Position of work unit u = qidx * (B * Hkv) + b * Hkv + kvh.
 struct UnitPos {
   int u, qidx, b, kvh;
 };
-DEVI UnitPos upos_first(const Params& p) {
+DEVI UnitPos upos_of(const Params& p, int u) {
   UnitPos x;
-  x.u = int(blockIdx.x);
+  x.u = u;
   const int bh_count = p.B * p.Hkv;
-  x.qidx = x.u / bh_count;
-  const int bh = x.u % bh_count;
+  x.qidx = u / bh_count;
+  const int bh = u - x.qidx * bh_count;
   x.b = bh / p.Hkv;
-  x.kvh = bh % p.Hkv;
+  x.kvh = bh - x.b * p.Hkv;
   return x;
 }
-DEVI void upos_next(UnitPos& x, const Params& p) {
-  x.u += int(gridDim.x);
-  x.kvh += p.step_kvh;
-  int carry = 0;
-  if (x.kvh >= p.Hkv) {
-    x.kvh -= p.Hkv;
-    carry = 1;
-  }
-  x.b += p.step_b + carry;
-  carry = 0;
-  if (x.b >= p.B) {
-    x.b -= p.B;
-    carry = 1;
-  }
-  x.qidx += p.step_q + carry;
-}
 
-// Key length of the unit's batch entry.  The load is volatile so that it is
-// issued where it is written (one unit ahead of its use) instead of being
-// moved next to its first use, which would expose its latency.
+// Key length of the unit's batch entry.
 DEVI int unit_len(const Params& p, const UnitPos& x) {
   if (!p.seqlens) return p.Sk;
   int v;
   asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p.seqlens + x.b));
   return v;
+}
+
+// Claims the next work unit of this launch (returns gridDim.x + a running
+// count).  Volatile so that it is issued where it is written, one unit ahead
+// of its use.
+DEVI int claim_unit(const Params& p) {
+  unsigned int v;
+  asm volatile("atom.global.add.u32 %0, [%1], 1;" : "=r"(v) : "l"(p.sched) : "memory");
+  return int(gridDim.x + v);
 }
 
 // Work unit -> (b, kvh, first token, key length, number of key tiles); len is
@@ -218,9 +216,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t drain = bar(2 * QB + 4 * S + 4 * kNQT);
   auto stg_free = [&](int t) { return bar(2 * QB + 4 * S + 4 * kNQT + 1 + t); };
   auto stg_full = [&](int t) { return bar(2 * QB + 4 * S + 5 * kNQT + 1 + t); };
+  auto uq_full = [&](int i) { return bar(2 * QB + 4 * S + 6 * kNQT + 1 + i); };
+  auto uq_empty = [&](int i) { return bar(2 * QB + 4 * S + 6 * kNQT + 1 + kUQ + i); };
+
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffTmemSlot);
   const uint64_t to = p.timeout_ns;
+  volatile int* uq = reinterpret_cast<volatile int*>(sbase + L::kOffUQ);   // [kUQ][2]: unit, key length
+  // Consumer side of the unit queue: entry k's (unit, key length), or
+  // n_units when the wait gave up.
+  auto next_unit = [&](uint32_t k, int& len, bool& ok) -> int {
+    const int i = int(k % kUQ);
+    ok = mbar_wait(uq_full(i), (k / kUQ) & 1, abort_flag, p.timeout_ns);
+    int u = p.n_units;
+    if (ok) {
+      u = uq[2 * i];
+      len = uq[2 * i + 1];
+    }
+    mbar_arrive(uq_empty(i));
+    return u;
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < QB; ++i) {
@@ -240,6 +255,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(o_free(t), 128);
       mbar_init(stg_free(t), 1);
       mbar_init(stg_full(t), 128);
+    }
+    for (int i = 0; i < kUQ; ++i) {
+      mbar_init(uq_full(i), 1);
+      mbar_init(uq_empty(i), kUQConsumers);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -271,13 +290,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       bool k_only = false;
       const uint32_t q_bytes = uint32_t(kNQT * L::kHalves * 64 * 2 * rows_per_tile);
-      UnitPos xn = upos_first(p);              // the grid never exceeds the unit count
-      int len_n = unit_len(p, xn);
-      for (UnitPos x = xn; ok && x.u < p.n_units; x = xn) {
-        const Unit U = unit_info(p, x, len_n);
-        // load the next unit's key length now, well before it is needed
-        upos_next(xn, p);
-        if (xn.u < p.n_units) len_n = unit_len(p, xn);
+      // Work units are claimed at run time (the first one is blockIdx.x; the
+      // grid never exceeds the unit count), one unit ahead, and published to
+      // the MMA and softmax warps through the unit queue; a unit index past
+      // the last unit ends every role's loop.
+      int u_next = int(blockIdx.x);
+      for (uint32_t k = 0; ok; ++k) {
+        const int u = u_next;
+        const int i = int(k % kUQ);
+        ok = mbar_wait(uq_empty(i), ((k / kUQ) & 1) ^ 1, abort_flag, to);
+        if (!ok) break;
+        const UnitPos x = upos_of(p, u < p.n_units ? u : 0);
+        const int len = (u < p.n_units) ? unit_len(p, x) : 0;
+        if (u < p.n_units) u_next = claim_unit(p);
+        uq[2 * i] = u;
+        uq[2 * i + 1] = len;
+        mbar_arrive(uq_full(i));        // release: the entry is visible to the consumers
+        if (u >= p.n_units) break;
+        const Unit U = unit_info(p, x, len);
         if (U.bad_len) raise_error(kErrBounds);
         if (U.n_tiles == 0) continue;
         const int qb = int(qn % QB);
@@ -370,13 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g_tile = 0;      // key tiles of earlier units (s_full / p_full phases)
       uint32_t qn = 0;          // units with work so far
       bool ok = true;
-      UnitPos xn = upos_first(p);              // the grid never exceeds the unit count
-      int len_n = unit_len(p, xn);
-      for (UnitPos x = xn; ok && x.u < p.n_units; x = xn) {
-        const Unit U = unit_info(p, x, len_n);
-        // load the next unit's key length now, well before it is needed
-        upos_next(xn, p);
-        if (xn.u < p.n_units) len_n = unit_len(p, xn);
+      for (uint32_t k = 0; ok; ++k) {
+        int len = 0;
+        const int u = next_unit(k, len, ok);
+        if (!ok || u >= p.n_units) break;
+        const Unit U = unit_info(p, upos_of(p, u), len);
         if (U.n_tiles == 0) continue;
         const int qb = int(qn % QB);
         const int s0 = int(kv_it % S);
@@ -451,12 +479,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool aborted = false;
 
     const int r_tok = r / p.G;   // token of this row within the Q tile
-    UnitPos xn = upos_first(p);
-    int len_n = unit_len(p, xn);
-    for (UnitPos x = xn; !aborted && x.u < p.n_units; x = xn) {
-      const Unit U = unit_info(p, x, len_n);
-      upos_next(xn, p);
-      if (xn.u < p.n_units) len_n = unit_len(p, xn);
+    for (uint32_t k = 0; !aborted; ++k) {
+      int len = 0;
+      bool qok;
+      const int u = next_unit(k, len, qok);
+      if (!__all_sync(0xffffffffu, qok)) {
+        aborted = true;
+        break;
+      }
+      if (u >= p.n_units) break;
+      const Unit U = unit_info(p, upos_of(p, u), len);
       const int token = U.q0 + t * p.Mq + r_tok;
       const bool row_ok = (r < rows_per_tile) && (token < p.Sq);
       int limit = 0;
@@ -704,6 +736,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMMA) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmCols);
+  }
+  if (threadIdx.x == 0) {
+    // every claim of this CTA is done: count it out; the last CTA resets the
+    // scheduler slot for the next launch that uses it
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
+    }
   }
 }
 

@@ -152,3 +152,19 @@ def test_out_of_range_length_reports_bounds_error_and_writes_zeros():
     assert gqa.gqa_device_status() == 0           # cleared by the read
     assert torch.all(out[1] == 0)
     assert torch.isneginf(lse[1]).all()
+
+
+def test_scheduler_slots_are_reset_between_launches():
+    """Work units are claimed from a per-launch counter slot that the launch's
+    last CTA resets; 130 launches reuse every slot twice and must keep giving
+    the same result, on grids of different sizes."""
+    small = to_dev(inputs.make_prefill(2, 8, 2, 300, 300, 64, seed=21, lens=(100, 300), dtype="bf16"))
+    big = to_dev(inputs.make_prefill(4, 12, 3, 600, 600, 64, seed=22, lens=(200, 600), dtype="bf16"))
+    ref_s = _run(small, 0.125, False)
+    ref_b = _run(big, 0.125, True)
+    for i in range(65):
+        out_s, _ = gqa.gqa_fwd(small["q"], small["k"], small["v"], seqlens_k=small["seqlens_k"], scale=0.125)
+        out_b, _ = gqa.gqa_fwd(big["q"], big["k"], big["v"], causal=True, seqlens_k=big["seqlens_k"], scale=0.125)
+    torch.cuda.synchronize()
+    assert gqa.gqa_device_status() == 0
+    assert torch.equal(out_s, ref_s[0]) and torch.equal(out_b, ref_b[0])
