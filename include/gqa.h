@@ -91,6 +91,10 @@ typedef enum {
  *   stream    cudaStream_t
  * bf16: D must be 64 or 128 and G = Hq/Hkv <= 128; q/k/v/out 16-byte aligned.
  * fp32: 1 <= D <= 256; 4-byte aligned.
+ * Concurrency (bf16): each call hands its work units out through one of 64
+ * counter slots in device memory, taken round-robin per call; up to 64 calls
+ * may be in flight on one device at once (on different streams), more must
+ * be serialised by the caller.
  * Returns GQA_OK, GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED or GQA_ERR_CUDA.
  */
 int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
