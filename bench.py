@@ -45,12 +45,12 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # profiles/prefill_kernel_d64_bert_base.md (one launch, bert_base)
     "prefill": {"source": "grouped_query_attention_08_b300/csrc/prefill_sm103.cuh",
-                "sha256": "c2e4626c5d03741fde20f8eaee84facd1726816a706742e5e2815e3b4d8bb501",
-                "workload": "bert_base", "bytes": 91089664},
+                "sha256": "60c6e71590358cf17e6a7aacaea55dff52137f4af9ee67e47182c188a7e2e689",
+                "workload": "bert_base", "bytes": 94938880},
     # profiles/decode_split_kernel_llama_decode_small.md (B=16 capture scaled to B=64 by KV bytes)
     "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh",
                "sha256": "1929d6fc61ce89c8eaa65031eb85b9fa679bfa8a328507b3a713dd2f30cf1f18",
-               "workload": "llama_decode", "bytes": 1269700000},
+               "workload": "llama_decode", "bytes": 1271500000},
 }
 
 
