@@ -49,8 +49,8 @@ NCU_TRAFFIC = {
                 "workload": "bert_base", "bytes": 94938880},
     # profiles/decode_split_kernel_llama_decode_small.md (B=16 capture scaled to B=64 by KV bytes)
     "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh",
-               "sha256": "1929d6fc61ce89c8eaa65031eb85b9fa679bfa8a328507b3a713dd2f30cf1f18",
-               "workload": "llama_decode", "bytes": 1271500000},
+               "sha256": "bdbf5370ee5f9909a3c8113f1991ca09478653442bedf0c446fbd2db9b8c7ef8",
+               "workload": "llama_decode", "bytes": 1275700000},
 }
 
 

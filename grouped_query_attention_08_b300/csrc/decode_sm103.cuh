@@ -14,11 +14,11 @@
 //    max / sum, and partial results merge exactly through their log-sum-exp.
 //
 // Split kernel: one CTA per (split, kvh, b), 4 warps.  Every warp walks
-// 16-key blocks of the split (block w, w+4, ...).  K and V rows are read
-// straight from global memory with 16-byte vector loads (one 16 B chunk = 8
-// consecutive head-dim values of one cached token); no shared-memory staging
-// is needed because the loads are placed directly in mma.sync fragment
-// order:
+// 16-key blocks of the split (block w, w+4, ...).  K and V rows stream from
+// global memory into a small per-warp shared-memory ring with 16-byte
+// asynchronous copies (cp.async, one 16 B chunk = 8 consecutive head-dim
+// values of one cached token), two or three blocks ahead of use, and are
+// read from there directly in mma.sync fragment order:
 //   S^T (16 keys x 8 heads) = K (16 x D) . Q^T (D x 8)   m16n8k16, K as A
 //   O^T (D x 8 heads)      += V^T (D x 16) . P^T (16 x 8) m16n8k16, V^T as A
 // The head-dimension index is permuted consistently between the K fragment
@@ -28,6 +28,8 @@
 // The work per byte is 8 flop/B, which would need ~52 TFLOP/s of fp32 FMA
 // at full HBM bandwidth, hence the tensor cores.
 #pragma once
+
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -84,27 +86,74 @@ struct BlockRegs {
   uint4 v[4][D / 64];   // V rows (2c, 2c+1, 2c+8, 2c+9), chunk 8*grp + r
 };
 
-// Loads one 16-key block starting at key `k0`; keys >= kend read as zero.
+// Shared-memory ring of one warp: kRing slots, each one 16-key block of K
+// rows then V rows, D*2 bytes per row.  The 16-byte chunk j of row `row` sits
+// at chunk position j ^ swz(row): with it, each quarter-warp of the fragment
+// reads below touches 8 distinct 16-byte bank groups (K: rows r, r+1 differ
+// in bit 2 of the swizzle; V: rows 2c + x, c = 0..3, differ in bits 1-2).
 template <int D>
-DEVI void load_block(BlockRegs<D>& R, const __nv_bfloat16* kbase, const __nv_bfloat16* vbase,
-                     size_t row_stride, int k0, int kend, int r, int c) {
-  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+struct Ring {
+  static constexpr int kRing = (D == 128) ? 3 : 4;       // blocks per warp (in flight: kRing - 1)
+  static constexpr uint32_t kRowBytes = D * 2;
+  static constexpr uint32_t kSlotBytes = 2 * kBlockKeys * kRowBytes;
+  static constexpr uint32_t kWarpBytes = kRing * kSlotBytes;
+  static constexpr uint32_t kBytes = kWarps * kWarpBytes;   // dynamic shared memory per CTA
+};
+
+DEVI uint32_t swz(int row) { return uint32_t((((row >> 1) & 3) << 1) ^ ((row & 1) << 2)); }
+
+DEVI void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+DEVI void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+// Starts the asynchronous copy of the 16-key block at key k0 into ring slot
+// `slot` (one commit group); keys >= kend are zero-filled (nothing is read
+// for them: their source is clamped to a valid row and 0 bytes are copied).
+template <int D>
+DEVI void issue_block(uint32_t slot, const __nv_bfloat16* kbase, const __nv_bfloat16* vbase, size_t row_stride,
+                      int k0, int kend, int kvalid, int lane) {
+  constexpr int kChunks = D / 8;                    // 16-byte chunks per row
+  constexpr int kPerLane = 2 * kBlockKeys * kChunks / 32;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int key = k0 + r + 8 * h;
-    const __nv_bfloat16* row = kbase + size_t(key) * row_stride;
-#pragma unroll
-    for (int q = 0; q < D / 32; ++q)
-      R.k[h][q] = (key < kend) ? ldg_stream(row + 8 * (c + 4 * q)) : z;
+  for (int i = 0; i < kPerLane; ++i) {
+    const int id = lane + 32 * i;
+    const int row = id / kChunks, chunk = id % kChunks;   // rows 0-15 K, 16-31 V
+    const int key = k0 + (row & (kBlockKeys - 1));
+    const bool ok = key < kend;
+    const __nv_bfloat16* src = (row < kBlockKeys ? kbase : vbase) + size_t(ok ? key : kvalid) * row_stride + 8 * chunk;
+    cp_async_16(slot + uint32_t(row) * Ring<D>::kRowBytes + (uint32_t(chunk) ^ swz(row)) * 16u, src, ok ? 16u : 0u);
   }
+  cp_async_commit();
+}
+
+DEVI uint4 lds128(uint32_t a) {
+  uint4 r;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "r"(a));
+  return r;
+}
+
+// Fragments of a block from its ring slot, in mma.sync operand order:
+// K rows (r, r+8) chunks c + 4q; V rows (2c, 2c+1, 2c+8, 2c+9) chunk 8 grp + r.
+template <int D>
+DEVI void fetch_block(BlockRegs<D>& R, uint32_t slot, int r, int c) {
+  constexpr uint32_t RB = Ring<D>::kRowBytes;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int key = k0 + 2 * c + (i & 1) + 8 * (i >> 1);
-    const __nv_bfloat16* row = vbase + size_t(key) * row_stride;
+  for (int h = 0; h < 2; ++h)
 #pragma unroll
-    for (int grp = 0; grp < D / 64; ++grp)
-      R.v[i][grp] = (key < kend) ? ldg_stream(row + 8 * (8 * grp + r)) : z;
-  }
+    for (int q = 0; q < D / 32; ++q) {
+      const int row = r + 8 * h;
+      R.k[h][q] = lds128(slot + uint32_t(row) * RB + (uint32_t(c + 4 * q) ^ swz(row)) * 16u);
+    }
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int grp = 0; grp < D / 64; ++grp) {
+      const int row = kBlockKeys + 2 * c + (i & 1) + 8 * (i >> 1);
+      R.v[i][grp] = lds128(slot + uint32_t(row) * RB + (uint32_t(8 * grp + r) ^ swz(row)) * 16u);
+    }
 }
 
 template <int D>
@@ -154,12 +203,35 @@ __global__ void __launch_bounds__(kThreads)
   for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
   float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;   // heads 2c and 2c+1
 
-  BlockRegs<D> cur, nxt;
-  int blk = warp;
-  if (blk < nblk) load_block<D>(cur, kbase, vbase, row_stride, kstart + blk * kBlockKeys, kend, r, c);
-  for (; blk < nblk; blk += kWarps) {
-    const int nb = blk + kWarps;
-    if (nb < nblk) load_block<D>(nxt, kbase, vbase, row_stride, kstart + nb * kBlockKeys, kend, r, c);
+  // This warp's blocks are warp, warp + 4, ...: kRing - 1 of them are always
+  // on their way from global memory into the warp's ring while one is used.
+  using RG = Ring<D>;
+  extern __shared__ __align__(16) uint8_t dsmem[];
+  const uint32_t ring = smem_u32(dsmem) + uint32_t(warp) * RG::kWarpBytes;
+#pragma unroll
+  for (int i = 0; i < RG::kRing - 1; ++i) {
+    const int bi = warp + i * kWarps;
+    if (bi < nblk)
+      issue_block<D>(ring + uint32_t(i) * RG::kSlotBytes, kbase, vbase, row_stride, kstart + bi * kBlockKeys, kend,
+                     kstart, lane);
+    else
+      cp_async_commit();     // keep one group per block position
+  }
+  BlockRegs<D> cur;
+  int it = 0;
+  for (int blk = warp; blk < nblk; blk += kWarps, ++it) {
+    cp_async_wait<RG::kRing - 2>();
+    __syncwarp();
+    fetch_block<D>(cur, ring + uint32_t(it % RG::kRing) * RG::kSlotBytes, r, c);
+    __syncwarp();            // every lane has read the slot refilled below (used one block ago)
+    {
+      const int nb = blk + (RG::kRing - 1) * kWarps;
+      const uint32_t slot = ring + uint32_t((it + RG::kRing - 1) % RG::kRing) * RG::kSlotBytes;
+      if (nb < nblk)
+        issue_block<D>(slot, kbase, vbase, row_stride, kstart + nb * kBlockKeys, kend, kstart, lane);
+      else
+        cp_async_commit();
+    }
     const int k0 = kstart + blk * kBlockKeys;
 
     // S^T = K . Q^T
@@ -208,8 +280,8 @@ __global__ void __launch_bounds__(kThreads)
       mma_bf16_16816(o[mt], __byte_perm(w0, w1, 0x5410), __byte_perm(w0, w1, 0x7632),
                      __byte_perm(w2, w3, 0x5410), __byte_perm(w2, w3, 0x7632), pb0, pb1);
     }
-    if (nb < nblk) cur = nxt;
   }
+  cp_async_wait<0>();
 
   // per-warp totals of l over the 8 lanes that share c
 #pragma unroll
@@ -218,10 +290,11 @@ __global__ void __launch_bounds__(kThreads)
     lB += __shfl_xor_sync(0xffffffffu, lB, off);
   }
 
-  // ---- combine the 4 warps through shared memory
-  __shared__ float s_o[kWarps][8][D];
-  __shared__ float s_m[kWarps][8];
-  __shared__ float s_l[kWarps][8];
+  // ---- combine the 4 warps through shared memory (the rings are done)
+  __syncthreads();
+  float (*s_o)[8][D] = reinterpret_cast<float (*)[8][D]>(dsmem);
+  float (*s_m)[8] = reinterpret_cast<float (*)[8]>(dsmem + sizeof(float) * kWarps * 8 * D);
+  float (*s_l)[8] = reinterpret_cast<float (*)[8]>(dsmem + sizeof(float) * (kWarps * 8 * D + kWarps * 8));
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     const int grp = mt >> 2, tt = mt & 3;
@@ -269,34 +342,79 @@ __global__ void __launch_bounds__(kThreads)
 // Log-sum-exp combine of split partials: one warp per (b, h).
 //   lse = ln sum_s exp(lse_s);  out = sum_s exp(lse_s - lse) * O_s
 // Splits whose start is at or past the sequence length were never written
-// and are skipped.  OutT is __nv_bfloat16 or float.
-template <typename OutT>
+// and are skipped.  The lanes first reduce the split lse values and leave the
+// normalised weights in shared memory; then each lane owns VEC consecutive
+// head-dim values (VEC = D / 32 for D = 64 / 128, else a strided loop with
+// VEC = 1) and reads every split's partial with independent vector loads.
+// OutT is __nv_bfloat16 or float.
+constexpr int kCombineMaxSplits = 128;
+
+template <typename OutT, int VEC>
 __global__ void __launch_bounds__(128)
     combine_kernel(const float* part_o, const float* part_lse, const int* seqlens, OutT* out,
                    int B, int Hq, int D, int nsplit, int split_len, int Smax) {
-  const int row = blockIdx.x * 4 + (threadIdx.x >> 5);
+  __shared__ float s_w[4][kCombineMaxSplits];
+  const int wib = threadIdx.x >> 5;
+  const int row = blockIdx.x * 4 + wib;
   const int lane = threadIdx.x & 31;
   if (row >= B * Hq) return;
   const int b = row / Hq;
   int Lb = seqlens[b];
   if (Lb < 0 || Lb > Smax) Lb = 0;
-  const int nvalid = min(nsplit, (Lb + split_len - 1) / split_len);
+  const int nvalid = min(min(nsplit, kCombineMaxSplits), (Lb + split_len - 1) / split_len);
   const float* lrow = part_lse + size_t(row) * nsplit;
   float M = -INFINITY;
-  for (int s = 0; s < nvalid; ++s) M = fmaxf(M, lrow[s]);
-  float W = 0.f;
+  for (int s = lane; s < nvalid; s += 32) M = fmaxf(M, lrow[s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   const float Mr = (M == -INFINITY) ? 0.f : M;
-  for (int s = 0; s < nvalid; ++s) W += expf(lrow[s] - Mr);
+  float W = 0.f;
+  for (int s = lane; s < nvalid; s += 32) {
+    const float e = expf(lrow[s] - Mr);
+    s_w[wib][s] = e;
+    W += e;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
+  __syncwarp();
   const float inv = W > 0.f ? 1.f / W : 0.f;
-  for (int d = lane; d < D; d += 32) {
-    float acc = 0.f;
-    for (int s = 0; s < nvalid; ++s)
-      acc += expf(lrow[s] - Mr) * part_o[(size_t(row) * nsplit + s) * D + d];
-    const float val = acc * inv;
-    if constexpr (sizeof(OutT) == 2)
-      out[size_t(row) * D + d] = __float2bfloat16_rn(val);
-    else
-      out[size_t(row) * D + d] = val;
+  const float* orow = part_o + size_t(row) * nsplit * D;
+  if constexpr (VEC > 1) {
+    // D == 32 * VEC: lane owns d = VEC*lane .. VEC*lane + VEC-1
+    using V = typename std::conditional<VEC == 4, float4, float2>::type;
+    float acc[VEC];
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+#pragma unroll 8
+    for (int s = 0; s < nvalid; ++s) {
+      const V x = __ldcs(reinterpret_cast<const V*>(orow + size_t(s) * D) + lane);
+      const float w = s_w[wib][s];
+      acc[0] += w * x.x;
+      acc[1] += w * x.y;
+      if constexpr (VEC == 4) {
+        acc[2] += w * x.z;
+        acc[3] += w * x.w;
+      }
+    }
+    OutT* o = out + size_t(row) * D + VEC * lane;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) {
+      if constexpr (sizeof(OutT) == 2)
+        o[e] = __float2bfloat16_rn(acc[e] * inv);
+      else
+        o[e] = acc[e] * inv;
+    }
+  } else {
+    for (int d = lane; d < D; d += 32) {
+      float acc = 0.f;
+#pragma unroll 8
+      for (int s = 0; s < nvalid; ++s) acc += s_w[wib][s] * __ldcs(orow + size_t(s) * D + d);
+      const float val = acc * inv;
+      if constexpr (sizeof(OutT) == 2)
+        out[size_t(row) * D + d] = __float2bfloat16_rn(val);
+      else
+        out[size_t(row) * D + d] = val;
+    }
   }
 }
 

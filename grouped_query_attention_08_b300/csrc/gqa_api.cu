@@ -170,6 +170,28 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
+// Dynamic shared memory of the decode split kernel: the warps' cp.async
+// rings, reused for the final merge of the warps.
+template <int D>
+constexpr int decode_smem_bytes() {
+  namespace dc = gqa::decode;
+  constexpr int ring = int(dc::Ring<D>::kBytes);
+  constexpr int merge = int(sizeof(float)) * (dc::kWarps * 8 * D + 2 * dc::kWarps * 8);
+  return ring > merge ? ring : merge;
+}
+
+bool decode_smem_attr_set(int dev) {
+  static bool done[kMaxDevices] = {false};
+  if (dev >= 0 && dev < kMaxDevices && done[dev]) return true;
+  if (cudaFuncSetAttribute(gqa::decode::decode_split_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           decode_smem_bytes<64>()) != cudaSuccess ||
+      cudaFuncSetAttribute(gqa::decode::decode_split_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           decode_smem_bytes<128>()) != cudaSuccess)
+    return false;
+  if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
+  return true;
+}
+
 int launch_f32(const gqa::f32::Params& p, cudaStream_t stream) {
   const long long rows = (long long)p.B * p.Hq * p.Sq;
   const long long gx = (rows + gqa::f32::kWarps - 1) / gqa::f32::kWarps;
@@ -328,15 +350,20 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
     p.split_len = sp.len;
     p.scale_log2 = scale * kLog2e;
     const dim3 grid(sp.n, Hkv, B);
+    if (!decode_smem_attr_set(current_device())) return GQA_ERR_CUDA;
     if (D == 64)
-      gqa::decode::decode_split_kernel<64><<<grid, gqa::decode::kThreads, 0, st>>>(p);
+      gqa::decode::decode_split_kernel<64><<<grid, gqa::decode::kThreads, decode_smem_bytes<64>(), st>>>(p);
     else
-      gqa::decode::decode_split_kernel<128><<<grid, gqa::decode::kThreads, 0, st>>>(p);
+      gqa::decode::decode_split_kernel<128><<<grid, gqa::decode::kThreads, decode_smem_bytes<128>(), st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     if (sp.n > 1) {
       const int rows = B * Hq;
-      gqa::decode::combine_kernel<__nv_bfloat16><<<(rows + 3) / 4, 128, 0, st>>>(
-          part_o, part_lse, cache_seqlens, static_cast<__nv_bfloat16*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
+      if (D == 128)
+        gqa::decode::combine_kernel<__nv_bfloat16, 4><<<(rows + 3) / 4, 128, 0, st>>>(
+            part_o, part_lse, cache_seqlens, static_cast<__nv_bfloat16*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
+      else
+        gqa::decode::combine_kernel<__nv_bfloat16, 2><<<(rows + 3) / 4, 128, 0, st>>>(
+            part_o, part_lse, cache_seqlens, static_cast<__nv_bfloat16*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
       if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     }
     return GQA_OK;
@@ -376,7 +403,7 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
     if (rc != GQA_OK) return rc;
     if (sp.n > 1) {
       const int rows = B * Hq;
-      gqa::decode::combine_kernel<float><<<(rows + 3) / 4, 128, 0, st>>>(
+      gqa::decode::combine_kernel<float, 1><<<(rows + 3) / 4, 128, 0, st>>>(
           part_o, part_lse, cache_seqlens, static_cast<float*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
       if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     }

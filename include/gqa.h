@@ -103,9 +103,10 @@ int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
 
 /*
  * gqa_decode_num_splits -- the number of KV-length splits gqa_decode will use.
- * num_splits > 0 is returned unchanged (clamped to 128 and to the number of
- * 16-key blocks of max_seqlen_k); num_splits <= 0 asks for the automatic
- * choice, which sizes the grid to fill the GPU of the current device.
+ * num_splits in 1..128 is returned clamped to the number of 16-key blocks of
+ * max_seqlen_k; num_splits <= 0 asks for the automatic choice, which sizes
+ * the grid to fill the GPU of the current device; num_splits > 128 is
+ * rejected (-GQA_ERR_INVALID_ARG).
  * Split s of every sequence covers keys [s*Ls, (s+1)*Ls) with
  * Ls = ceil(max_seqlen_k / n) rounded up to 16 ([GQA-BERT] "阶段二":
  * num_splits cuts the key range into pieces computed independently).
@@ -144,8 +145,9 @@ size_t gqa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits,
  *                  Caller-owned; must not be used by another call in flight.
  *   workspace_bytes its size
  *   stream         cudaStream_t
- * bf16: D must be 64 or 128 and G <= 16.  The new token sees the whole
- * cached prefix (no causal term).
+ * bf16: D must be 64 or 128 and G <= 8 (GQA_ERR_UNSUPPORTED otherwise).
+ * fp32: 1 <= D <= 256.  The new token sees the whole cached prefix (no
+ * causal term).
  */
 int gqa_decode(const void* q, const void* kcache, const void* vcache,
                const int* cache_seqlens, void* out, int B, int Hq, int Hkv, int D,
