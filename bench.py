@@ -45,8 +45,8 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # profiles/prefill_kernel_d64_bert_base.md (one launch, bert_base)
     "prefill": {"source": "grouped_query_attention_08_b300/csrc/prefill_sm103.cuh",
-                "sha256": "60c6e71590358cf17e6a7aacaea55dff52137f4af9ee67e47182c188a7e2e689",
-                "workload": "bert_base", "bytes": 94938880},
+                "sha256": "5ef35b9783edf6b9c32a946777bf59011fc0944f53dd5a00606698e03fb60c04",
+                "workload": "bert_base", "bytes": 94361088},
     # profiles/decode_split_kernel_llama_decode_small.md (B=16 capture scaled to B=64 by KV bytes)
     "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh",
                "sha256": "bdbf5370ee5f9909a3c8113f1991ca09478653442bedf0c446fbd2db9b8c7ef8",

@@ -23,31 +23,39 @@
 //   warps 0-3  softmax + epilogue for Q tile 0 (thread = one row = one TMEM lane)
 //   warps 4-7  softmax + epilogue for Q tile 1
 //   warp  8    TMA producer: the unit's Q tiles, then a K ring and a V ring
-//   warp  9    MMA issuer: S_t = Q_t K^T into TMEM, O_t += P_t V with P_t
-//              read from TMEM (P overwrites S_t as packed bf16)
-//   warps 10-11 idle (they complete the third warpgroup, which hands its
+//   warp  9    MMA issuer for Q tile 0, warp 10 for Q tile 1: S_t = Q_t K^T
+//              into TMEM, O_t += P_t V with P_t read from TMEM
+//   warp  11   idle (it completes the third warpgroup, which hands its
 //              registers to the softmax warpgroups with setmaxnreg)
 // TMEM (512 columns): S0 [0,128) S1 [128,256) O0 [256,256+D) O1 [256+D,256+2D),
 // and with D = 64 the unit's Q tiles Q0 [384,416) Q1 [416,448) as bf16 pairs.
-// The two softmax warpgroups ping-pong: while one computes exponentials the
-// tensor core runs the other's PV and next QK^T.  Across units, the MMA warp
-// starts the next unit's QK^T while the softmax warps are still writing the
-// previous unit's output (S and O are separate TMEM regions); only the first
-// PV of a unit waits for the previous epilogue to have read O_t.  With D = 64
-// QK^T takes Q from TMEM: a tensor-core MMA can read about 64 bytes of shared
-// memory per clock, which two shared-memory operands of a 128x128x16 step
-// exceed by a factor of two, while an operand in TMEM does not count against
-// it; the copy also frees the Q buffer at the start of each unit, so the next
-// unit's Q lands during the current one.
 //
-// Softmax details: t = s * scale * log2(e).  Exponents are taken in one pass
-// against a reference max (the running max; for a row's first tile the max of
-// its first 8 admissible scores), which may be below the true max: the final
-// division by l = sum p is exact for any reference.  The pass is kept when the
-// tile's row sum stays below 2^20 (so no p exceeds it); otherwise the tile is
-// redone against its true max, and the running max moves only when it grows
-// by more than 8 (log2 units).  Masked keys (j >= L_b, or j > i + Sk - Sq when
-// causal) get p = 0 exactly.
+// Schedule of Q tile t (key tiles j of a unit):
+//   issuer:  QK_t(0), QK_t(1), then per j: PV_t(j), QK_t(j+2)
+//   softmax: per j: P_t(j) from S_t(j) in registers; read S_t(j+1) into
+//            registers; write P_t(j) (packed bf16) over S_t
+// so S_t(j+1) is computed while the softmax works on tile j, and the softmax
+// never waits for its own tile's matrix products in the steady state.
+// QK_t(j+2) may overwrite S_t once PV_t(j) has read P_t(j): both come from the
+// same issuing thread, so the tensor core runs them in that order.  One
+// issuing thread per Q tile lets each thread's barrier waits overlap the
+// other's MMAs.  Buffers shared by the two Q tiles (the Q set, the K/V ring
+// stages) are released by both issuers.  Across units, an issuer starts the
+// next unit's QK^T right after its last PV; only the first PV of a unit
+// waits for the previous epilogue to have read O_t.  With D = 64 QK^T takes Q
+// from TMEM: a tensor-core MMA can read about 64 bytes of shared memory per
+// clock, which two shared-memory operands of a 128x128x16 step exceed by a
+// factor of two, while an operand in TMEM does not count against it; the
+// copy also frees the Q buffer at the start of each unit, so the next unit's
+// Q lands during the current one.  Hand-offs where a whole warp takes part
+// use one elected arrival per warp (fewer shared-memory atomics).
+//
+// Softmax details: t = s * scale * log2(e).  Each tile's row max is taken
+// first, then the exponents against the reference max m, which moves only
+// when the row max grows by more than 8 (log2 units), so p <= 2^8 and O_t is
+// rescaled only then (after PV_t(j-1) has completed); the final division by
+// l = sum p is exact for any reference.  Masked keys (j >= L_b, or
+// j > i + Sk - Sq when causal) get p = 0 exactly.
 #pragma once
 
 #include "common.cuh"
@@ -59,18 +67,17 @@ constexpr int kBM = 128;       // rows per Q tile (= TMEM lanes)
 constexpr int kBN = 128;       // keys per K/V tile
 constexpr int kNQT = 2;        // Q tiles per work unit
 constexpr int kWarpTMA = 8;
-constexpr int kWarpMMA = 9;
+constexpr int kWarpMMA = 9;      // issues the MMAs of Q tile 0
+constexpr int kWarpMMA2 = 10;    // issues the MMAs of Q tile 1
 constexpr int kThreads = 384;
 constexpr int kSoftmaxRegs = 216;   // 2 x 128 x 216 + 128 x 72 = 384 x 168 registers at launch
 constexpr int kLaunchRegs = 168;
 constexpr int kOtherRegs = 72;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kUQ = 4;                // depth of the shared-memory work-unit queue
-// consumers of a queue entry: the MMA-issuing thread and every softmax thread
-constexpr uint32_t kUQConsumers = 1 + kNQT * 128;
-// A one-pass tile is kept while its row sum stays below this (2^20): then no
-// probability exceeds 2^20 and the fp32 accumulators stay far from overflow.
-constexpr float kOnePassSumLimit = 1048576.0f;
+// consumers of a queue entry: the two MMA-issuing threads and every softmax
+// warp (one elected arrival per warp)
+constexpr uint32_t kUQConsumers = kNQT + kNQT * 4;
 
 template <int D>
 struct Layout {
@@ -93,8 +100,8 @@ struct Layout {
   static constexpr uint32_t kOffBar = kOffOut + kNQT * kHalfBytes;
   // barriers: q_full[QB], q_empty[QB], k_full[S], k_empty[S], v_full[S], v_empty[S],
   //           s_full[2], p_full[2], o_done[2], o_free[2], drain, stg_free[2], stg_full[2],
-  //           uq_full[kUQ], uq_empty[kUQ]
-  static constexpr int kNumBars = 2 * kQBufs + 4 * kStages + 4 * kNQT + 1 + 2 * kNQT + 2 * kUQ;
+  //           uq_full[kUQ], uq_empty[kUQ], s_free[2], pv_done[2], drain2
+  static constexpr int kNumBars = 2 * kQBufs + 4 * kStages + 4 * kNQT + 1 + 2 * kNQT + 2 * kUQ + 2 * kNQT + 1;
   // unit queue: kUQ entries of (unit index, key length)
   static constexpr uint32_t kOffUQ = kOffBar + 8u * kNumBars;
   static constexpr uint32_t kOffTmemSlot = kOffUQ + 8u * kUQ;
@@ -218,14 +225,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto stg_full = [&](int t) { return bar(2 * QB + 4 * S + 5 * kNQT + 1 + t); };
   auto uq_full = [&](int i) { return bar(2 * QB + 4 * S + 6 * kNQT + 1 + i); };
   auto uq_empty = [&](int i) { return bar(2 * QB + 4 * S + 6 * kNQT + 1 + kUQ + i); };
+  auto s_free = [&](int t) { return bar(2 * QB + 4 * S + 6 * kNQT + 1 + 2 * kUQ + t); };
+  auto pv_done = [&](int t) { return bar(2 * QB + 4 * S + 7 * kNQT + 1 + 2 * kUQ + t); };
+  const uint32_t drain2 = bar(2 * QB + 4 * S + 8 * kNQT + 1 + 2 * kUQ);
 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffTmemSlot);
   const uint64_t to = p.timeout_ns;
   volatile int* uq = reinterpret_cast<volatile int*>(sbase + L::kOffUQ);   // [kUQ][2]: unit, key length
   // Consumer side of the unit queue: entry k's (unit, key length), or
-  // n_units when the wait gave up.
-  auto next_unit = [&](uint32_t k, int& len, bool& ok) -> int {
+  // n_units when the wait gave up.  A whole warp (softmax) releases the
+  // entry with one arrival once every lane has read it; a single thread
+  // (MMA issuer) arrives itself.
+  auto next_unit = [&](uint32_t k, int& len, bool& ok, bool whole_warp) -> int {
     const int i = int(k % kUQ);
     ok = mbar_wait(uq_full(i), (k / kUQ) & 1, abort_flag, p.timeout_ns);
     int u = p.n_units;
@@ -233,34 +245,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       u = uq[2 * i];
       len = uq[2 * i + 1];
     }
-    mbar_arrive(uq_empty(i));
+    if (whole_warp) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(uq_empty(i));
+    } else {
+      mbar_arrive(uq_empty(i));
+    }
     return u;
   };
 
   if (threadIdx.x == 0) {
+    // buffers shared by the Q tiles are released by both MMA-issuing threads
     for (int i = 0; i < QB; ++i) {
       mbar_init(q_full(i), 1);
-      mbar_init(q_empty(i), 1);
+      mbar_init(q_empty(i), kNQT);
     }
     for (int s = 0; s < S; ++s) {
       mbar_init(k_full(s), 1);
-      mbar_init(k_empty(s), 1);
+      mbar_init(k_empty(s), kNQT);
       mbar_init(v_full(s), 1);
-      mbar_init(v_empty(s), 1);
+      mbar_init(v_empty(s), kNQT);
     }
     for (int t = 0; t < kNQT; ++t) {
       mbar_init(s_full(t), 1);
-      mbar_init(p_full(t), 128);
+      mbar_init(p_full(t), 4);         // one arrival per softmax warp of the tile
+      mbar_init(s_free(t), 4);
+      mbar_init(pv_done(t), 1);
       mbar_init(o_done(t), 1);
-      mbar_init(o_free(t), 128);
+      mbar_init(o_free(t), 4);
       mbar_init(stg_free(t), 1);
-      mbar_init(stg_full(t), 128);
+      mbar_init(stg_full(t), 4);
     }
     for (int i = 0; i < kUQ; ++i) {
       mbar_init(uq_full(i), 1);
       mbar_init(uq_empty(i), kUQConsumers);
     }
     mbar_init(drain, 1);
+    mbar_init(drain2, 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -354,9 +375,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (qn > 0) mbar_wait(q_full(int((qn - 1) % QB)), ((qn - 1) / QB) & 1, &no_abort, 200000000ull);
       }
     }
-  } else if (warp == kWarpMMA) {
-    // ---------------------------------------------------------- MMA issuer
+  } else if (warp == kWarpMMA || warp == kWarpMMA2) {
+    // --------------------------------------------------------- MMA issuers
+    // One thread per Q tile t issues that tile's MMAs in the order
+    //   QK_t(0), QK_t(1), then per key tile j: PV_t(j), QK_t(j+2).
+    // P_t(j) is written over S_t once the softmax has read S_t(j+1) into
+    // registers, so S_t(j+1) is computed while the softmax works on tile j,
+    // and QK_t(j+2) may overwrite S_t as soon as PV_t(j) has read P_t(j)
+    // (same thread, so in order).  The two threads' barrier waits overlap
+    // each other's MMAs.
     if (lane == 0) {
+      const int tq = warp - kWarpMMA;
       const uint32_t idesc_s = make_idesc_bf16(128, kBN, 0, 0);   // Q, K both K-major
       const uint32_t idesc_o = make_idesc_bf16(128, D, 0, 1);     // P (TMEM), V MN-major
       auto issue_s = [&](int t, int qb, int s) {
@@ -376,15 +405,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // D = 64: the unit's Q tiles from shared memory into TMEM (executes
       // after every MMA issued before it, so the previous unit's QK^T are done)
-      auto copy_q = [&](int qb) {
+      auto copy_q = [&](int qb, int t) {
+        const uint32_t qa = base + L::kOffQ + qb * L::kQSetBytes + t * L::kTileBytes;
 #pragma unroll
-        for (int t = 0; t < kNQT; ++t) {
-          const uint32_t qa = base + L::kOffQ + qb * L::kQSetBytes + t * L::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            tmem_cp_128x256b(tmem + (t ? L::kTmQ1 : L::kTmQ0) + uint32_t(ks) * 8u,
-                             make_sdesc_sw128(qa + uint32_t(ks) * 32u, 16, 1024));
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          tmem_cp_128x256b(tmem + (t ? L::kTmQ1 : L::kTmQ0) + uint32_t(ks) * 8u,
+                           make_sdesc_sw128(qa + uint32_t(ks) * 32u, 16, 1024));
       };
       auto issue_pv = [&](int t, int s, bool acc) {
         const uint32_t va = base + L::kOffV + s * L::kTileBytes;
@@ -396,68 +422,64 @@ __global__ void __launch_bounds__(kThreads, 1)
                   idesc_o, (acc || ks > 0) ? 1u : 0u);
         }
       };
-      uint32_t kv_it = 0;       // K/V tiles consumed so far
-      uint32_t g_tile = 0;      // key tiles of earlier units (s_full / p_full phases)
+      uint32_t g = 0;           // key tiles of earlier units (K/V ring position; s_full / p_full phases)
       uint32_t qn = 0;          // units with work so far
+      uint32_t n2 = 0;          // units with two or more key tiles so far (s_free / pv_done phases)
       bool ok = true;
       for (uint32_t k = 0; ok; ++k) {
         int len = 0;
-        const int u = next_unit(k, len, ok);
+        const int u = next_unit(k, len, ok, false);
         if (!ok || u >= p.n_units) break;
         const Unit U = unit_info(p, upos_of(p, u), len);
-        if (U.n_tiles == 0) continue;
+        const int n = U.n_tiles;
+        if (n == 0) continue;
         const int qb = int(qn % QB);
-        const int s0 = int(kv_it % S);
-        ok = mbar_wait(q_full(qb), (qn / QB) & 1, abort_flag, to) &&
-             mbar_wait(k_full(s0), (kv_it / S) & 1, abort_flag, to);
+        // QK^T_t of the unit's key tile jj, K from ring stage (g + jj) % S
+        auto qk = [&](int jj) -> bool {
+          const uint32_t it = g + uint32_t(jj);
+          const int s = int(it % S);
+          if (!mbar_wait(k_full(s), (it / S) & 1, abort_flag, to)) return false;
+          tc_fence_after();
+          issue_s(tq, qb, s);
+          umma_commit(s_full(tq));
+          umma_commit(k_empty(s));
+          if (!L::kQInTmem && jj == n - 1) umma_commit(q_empty(qb));   // the unit's last read of Q
+          return true;
+        };
+        ok = mbar_wait(q_full(qb), (qn / QB) & 1, abort_flag, to);
         if (!ok) break;
         tc_fence_after();
         if constexpr (L::kQInTmem) {
-          copy_q(qb);
-          umma_commit(q_empty(qb));     // the Q buffer is free once the copies land
+          copy_q(qb, tq);
+          umma_commit(q_empty(qb));     // this Q tile's part of the buffer is free once copied
         }
-        for (int t = 0; t < kNQT; ++t) {
-          issue_s(t, qb, s0);
-          umma_commit(s_full(t));
-        }
-        umma_commit(k_empty(s0));
-        if (!L::kQInTmem && U.n_tiles == 1) umma_commit(q_empty(qb));
-        for (int j = 0; ok && j < U.n_tiles; ++j) {
-          const uint32_t it = kv_it + j;
+        ok = qk(0);
+        // S_t(1) may overwrite S_t(0) once the softmax has read it
+        if (ok && n >= 2) ok = mbar_wait(s_free(tq), n2 & 1, abort_flag, to) && qk(1);
+        for (int j = 0; ok && j < n; ++j) {
+          const uint32_t it = g + uint32_t(j);
           const int s = int(it % S);
-          const uint32_t ph = (it / S) & 1;
-          const bool has_next = j + 1 < U.n_tiles;
-          const int ns = int((it + 1) % S);
-          const uint32_t nph = ((it + 1) / S) & 1;
-          ok = mbar_wait(v_full(s), ph, abort_flag, to);
-          if (ok && has_next) ok = mbar_wait(k_full(ns), nph, abort_flag, to);
-          for (int t = 0; ok && t < kNQT; ++t) {
-            ok = mbar_wait(p_full(t), (g_tile + j) & 1, abort_flag, to);
-            // the unit's first PV overwrites O_t: the previous epilogue must have read it
-            if (ok && j == 0 && qn > 0) ok = mbar_wait(o_free(t), (qn - 1) & 1, abort_flag, to);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(t, s, j > 0);
-            if (!has_next) umma_commit(o_done(t));
-            if (has_next) {
-              issue_s(t, qb, ns);
-              umma_commit(s_full(t));
-            }
-          }
+          ok = mbar_wait(v_full(s), (it / S) & 1, abort_flag, to) && mbar_wait(p_full(tq), it & 1, abort_flag, to);
+          // the unit's first PV overwrites O_t: the previous epilogue must have read it
+          if (ok && j == 0 && qn > 0) ok = mbar_wait(o_free(tq), (qn - 1) & 1, abort_flag, to);
           if (!ok) break;
+          tc_fence_after();
+          issue_pv(tq, s, j > 0);
+          if (j == n - 2) umma_commit(pv_done(tq));   // lets the softmax rescale O_t before the last PV
+          if (j == n - 1) umma_commit(o_done(tq));
           umma_commit(v_empty(s));
-          if (has_next) umma_commit(k_empty(ns));
-          if (!L::kQInTmem && j + 2 == U.n_tiles) umma_commit(q_empty(qb));   // the unit's last QK^T is issued
+          if (j + 2 < n) ok = qk(j + 2);
         }
-        kv_it += U.n_tiles;
-        g_tile += U.n_tiles;
+        if (n >= 2) ++n2;
+        g += uint32_t(n);
         ++qn;
       }
       if (!ok) {
-        // aborted: wait for the tensor core to finish what was issued
+        // aborted: wait for the tensor core to finish what this thread issued
         volatile int no_abort = 0;
-        umma_commit(drain);
-        mbar_wait(drain, 0, &no_abort, 200000000ull);
+        const uint32_t db = tq ? drain2 : drain;
+        umma_commit(db);
+        mbar_wait(db, 0, &no_abort, 200000000ull);
       }
     }
   }
@@ -475,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t c2 = f2_pack(c, c);
     uint32_t g_tile = 0;
     uint32_t qn = 0;
+    uint32_t n2 = 0;          // units with two or more key tiles so far
     uint32_t n_stage = 0;     // uses of this tile's staging block so far
     bool aborted = false;
 
@@ -482,7 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (uint32_t k = 0; !aborted; ++k) {
       int len = 0;
       bool qok;
-      const int u = next_unit(k, len, qok);
+      const int u = next_unit(k, len, qok, true);
       if (!__all_sync(0xffffffffu, qok)) {
         aborted = true;
         break;
@@ -500,147 +523,129 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m = -INFINITY;
       float l = 0.f;
 
-      for (int j = 0; j < U.n_tiles; ++j) {
-        const bool ok = mbar_wait(s_full(t), (g_tile + j) & 1, abort_flag, to);
-        if (!__all_sync(0xffffffffu, ok)) {
-          aborted = true;
-          break;
-        }
+      const int n = U.n_tiles;
+      uint32_t sv[kBN];        // S_t of the current key tile, in registers
+      if (n > 0) {
+        // S_t(0), read before the loop so that every tile's S is visibly
+        // defined on entry (S_t(j+1) is read at the end of tile j)
+        // (loaded even after a failed wait, whose tile is then skipped)
+        const bool ok = mbar_wait(s_full(t), g_tile & 1, abort_flag, to);
+        if (!__all_sync(0xffffffffu, ok)) aborted = true;
         tc_fence_after();
-        uint32_t sv[kBN];
         tmem_ld_32x32b_x32(tS + 0, sv + 0);
         tmem_ld_32x32b_x32(tS + 32, sv + 32);
         tmem_ld_32x32b_x32(tS + 64, sv + 64);
         tmem_ld_32x32b_x32(tS + 96, sv + 96);
         tmem_ld_wait_x128(sv);
+        if (n >= 2 && !aborted) {
+          // S_t(0) is in registers: QK_t(1) may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free(t));
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < kBN; ++i) sv[i] = 0u;
+      }
+      for (int j = 0; j < n && !aborted; ++j) {
+        const uint32_t gi = g_tile + uint32_t(j);
+        uint32_t pall[kBN / 2];  // P_t(j) as bf16 pairs, written to TMEM at the end of the tile
+        // Before P_t(j) can go over S_t: S_t(j+1) must be complete (it is
+        // then read into registers), or for the unit's last tile PV_t(j-1).
+        // Either way PV_t(j-1) has completed (QK_t(j+1) was issued after
+        // it), which also allows rescaling O_t.
+        bool waited = false;
+        auto wait_next = [&]() -> bool {
+          if (waited) return true;
+          waited = true;
+          bool okn = true;
+          if (j + 1 < n)
+            okn = mbar_wait(s_full(t), (gi + 1) & 1, abort_flag, to);
+          else if (n >= 2)
+            okn = mbar_wait(pv_done(t), n2 & 1, abort_flag, to);
+          okn = __all_sync(0xffffffffu, okn);
+          tc_fence_after();
+          return okn;
+        };
 
         const int lim = limit - j * kBN;
-        // Every key of the tile admissible for every row of the warp and a
-        // positive scale: no mask is needed and the max can be taken on the
-        // raw scores.  Rows that hold no query (past the tile's G * Mq rows or
-        // past Sq) are never stored, so they neither force the masked path nor
-        // vote for a second pass.  Every branch below is warp-uniform because
-        // each ends in tcgen05.st, which the whole warp executes together.
-        const bool fast = __all_sync(0xffffffffu, lim >= kBN || !row_ok) && (c > 0.f);
-        uint64_t acc0 = 0ull, acc1 = 0ull;       // packed (+0.0f, +0.0f) row sums
-        bool done = false;
-        if (c > 0.f) {
-          // One pass against a reference max: the running max m, or for a
-          // row's first tile the max of its first 8 admissible scores.  The
-          // reference may sit below the true max; that is exact after the
-          // final division as long as no p grows large, so the pass is kept
-          // when the tile's row sum stays below kOnePassSumLimit (no p can
-          // exceed it) and is redone against the true max otherwise.
-          float mref = m;
-          if (m == -INFINITY) {
-            float m8 = -INFINITY;
+        // Keys at or past the row's limit get exactly zero weight.  When every
+        // row of the warp admits every key of the tile (rows that hold no
+        // query are never stored and do not count) and the scale is positive,
+        // no mask is needed and the max is taken on the raw scores.  Every
+        // branch below is warp-uniform.
+        const bool full = __all_sync(0xffffffffu, lim >= kBN || !row_ok) && (c > 0.f);
+        float mt = -INFINITY;
+        if (full) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (i < lim) m8 = fmaxf(m8, __uint_as_float(sv[i]));
-            mref = (m8 == -INFINITY) ? 0.f : m8 * c;
-          }
-          const uint64_t nm2 = f2_pack(-mref, -mref);
-          if (fast) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int k0 = q * 32 + 2 * i;
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), c2, nm2), x0, x1);
-                const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                if (i & 1)
-                  acc1 = f2_add(acc1, f2_pack(p0, p1));
-                else
-                  acc0 = f2_add(acc0, f2_pack(p0, p1));
-                pk[i] = pack_bf16x2(p0, p1);
-              }
-              tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
-            }
-          } else {
-            // edge tile: keys at or past the row's limit get exactly zero weight
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int k0 = q * 32 + 2 * i;
-                float x0, x1;
-                f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), c2, nm2), x0, x1);
-                const float p0 = ex2_approx(k0 < lim ? x0 : -INFINITY);
-                const float p1 = ex2_approx(k0 + 1 < lim ? x1 : -INFINITY);
-                if (i & 1)
-                  acc1 = f2_add(acc1, f2_pack(p0, p1));
-                else
-                  acc0 = f2_add(acc0, f2_pack(p0, p1));
-                pk[i] = pack_bf16x2(p0, p1);
-              }
-              tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
-            }
-          }
-          float t0, t1;
-          f2_unpack(f2_add(acc0, acc1), t0, t1);
-          const float tile_sum = t0 + t1;
-          done = !__any_sync(0xffffffffu, row_ok && !(tile_sum <= kOnePassSumLimit));
-          if (done && m == -INFINITY && tile_sum > 0.f) m = mref;
-        }
-        if (!done) {
-          // Two passes: the tile max first, then the exponents (a non-positive
-          // scale, or a tile whose scores rose far above the reference).
-          acc0 = 0ull;
-          acc1 = 0ull;
-          float mt = -INFINITY;
+          for (int i = 0; i < kBN; i += 2) mt = fmax3(mt, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+          mt *= c;
+        } else {
 #pragma unroll
           for (int i = 0; i < kBN; ++i) {
             const float f = (i < lim) ? __uint_as_float(sv[i]) * c : -INFINITY;
             sv[i] = __float_as_uint(f);
             mt = fmaxf(mt, f);
           }
-          const float m_new = fmaxf(m, mt);
-          const bool need = m_new > m + kRescaleThreshold;
-          float alpha = 1.f;
-          if (need) {
-            alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
-            l *= alpha;
-            m = m_new;
+        }
+        // the reference max moves only when the row max grows by more than
+        // the threshold (then p <= 2^threshold below it)
+        const float m_new = fmaxf(m, mt);
+        const bool need = m_new > m + kRescaleThreshold;
+        float alpha = 1.f;
+        if (need) {
+          alpha = (m == -INFINITY) ? 0.f : ex2_approx(m - m_new);
+          l *= alpha;
+          m = m_new;
+        }
+        if (__any_sync(0xffffffffu, need && j > 0)) {
+          if (!wait_next()) {
+            aborted = true;
+            break;
           }
-          if (__any_sync(0xffffffffu, need && j > 0)) {
-            // move O_t to the new reference maximum.  The previous PV has
-            // completed: this tile's S was committed after it.
+          // move O_t to the new reference maximum
 #pragma unroll
-            for (int cc = 0; cc < D; cc += 32) {
-              uint32_t o[32];
-              tmem_ld_32x32b_x32(tO + cc, o);
-              tmem_ld_wait_x32(o);
-              const uint64_t al2 = f2_pack(alpha, alpha);
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t o[32];
+            tmem_ld_32x32b_x32(tO + cc, o);
+            tmem_ld_wait_x32(o);
+            const uint64_t al2 = f2_pack(alpha, alpha);
 #pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                const uint64_t v = f2_fma(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), al2, 0ull);
-                float lo, hi;
-                f2_unpack(v, lo, hi);
-                o[i] = __float_as_uint(lo);
-                o[i + 1] = __float_as_uint(hi);
-              }
-              tmem_st_32x32b_x32(tO + cc, o);
+            for (int i = 0; i < 32; i += 2) {
+              const uint64_t v = f2_fma(f2_pack(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), al2, 0ull);
+              float lo, hi;
+              f2_unpack(v, lo, hi);
+              o[i] = __float_as_uint(lo);
+              o[i + 1] = __float_as_uint(hi);
             }
+            tmem_st_32x32b_x32(tO + cc, o);
           }
-          const float mref = (m == -INFINITY) ? 0.f : m;
+        }
+        const float mref = (m == -INFINITY) ? 0.f : m;
+        uint64_t acc0 = 0ull, acc1 = 0ull;       // packed (+0.0f, +0.0f) row sums
+        if (full) {
+          const uint64_t nm2 = f2_pack(-mref, -mref);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t pk[16];
+          for (int i = 0; i < kBN / 2; ++i) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), c2, nm2), x0, x1);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (i & 1)
+              acc1 = f2_add(acc1, f2_pack(p0, p1));
+            else
+              acc0 = f2_add(acc0, f2_pack(p0, p1));
+            pall[i] = pack_bf16x2(p0, p1);
+          }
+        } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int k0 = q * 32 + 2 * i;
-              const float p0 = ex2_approx(__uint_as_float(sv[k0]) - mref);
-              const float p1 = ex2_approx(__uint_as_float(sv[k0 + 1]) - mref);
-              if (i & 1)
-                acc1 = f2_add(acc1, f2_pack(p0, p1));
-              else
-                acc0 = f2_add(acc0, f2_pack(p0, p1));
-              pk[i] = pack_bf16x2(p0, p1);
-            }
-            tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pk);
+          for (int i = 0; i < kBN / 2; ++i) {
+            const float p0 = ex2_approx(__uint_as_float(sv[2 * i]) - mref);
+            const float p1 = ex2_approx(__uint_as_float(sv[2 * i + 1]) - mref);
+            if (i & 1)
+              acc1 = f2_add(acc1, f2_pack(p0, p1));
+            else
+              acc0 = f2_add(acc0, f2_pack(p0, p1));
+            pall[i] = pack_bf16x2(p0, p1);
           }
         }
         {
@@ -648,9 +653,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           f2_unpack(f2_add(acc0, acc1), s0, s1);
           l += s0 + s1;
         }
+        if (!wait_next()) {
+          aborted = true;
+          break;
+        }
+        // Hand-off: S_t(j+1)'s first 64 columns into registers, P_t(j) over
+        // them (bf16 pairs fill exactly 64 columns), then the other 64.
+        if (j + 1 < n) {
+          tmem_ld_32x32b_x32(tS + 0, sv + 0);
+          tmem_ld_32x32b_x32(tS + 32, sv + 32);
+          tmem_ld_wait_x32(sv);
+          tmem_ld_wait_x32(sv + 32);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pall + q * 16);
+        if (j + 1 < n) {
+          tmem_ld_32x32b_x32(tS + 64, sv + 64);
+          tmem_ld_32x32b_x32(tS + 96, sv + 96);
+          tmem_ld_wait_x32(sv + 64);
+          tmem_ld_wait_x32(sv + 96);
+        }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(p_full(t));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full(t));
       }
 
       // ---------------------------------------------------------- epilogue
@@ -671,7 +697,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld_wait_x32(o), tmem_ld_wait_x32(o + 32);
         // O_t has been read: the next unit's first PV may overwrite it
         tc_fence_before();
-        mbar_arrive(o_free(t));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(o_free(t));
       } else {
 #pragma unroll
         for (int i = 0; i < D; ++i) o[i] = 0u;
@@ -695,7 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bulk_wait_read_all();        // the previous store has finished reading the block
             mbar_arrive(stg_free(t));
           }
-          bool ok = mbar_wait(stg_free(t), ph, abort_flag, to);
+          const bool ok = __all_sync(0xffffffffu, mbar_wait(stg_free(t), ph, abort_flag, to));
           if (ok) {
 #pragma unroll
             for (int c8 = 0; c8 < 8; ++c8) {
@@ -711,7 +738,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                            : "memory");
             }
             fence_proxy_async_smem();
-            mbar_arrive(stg_full(t));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(stg_full(t));
           }
           if (leader && ok && mbar_wait(stg_full(t), ph, abort_flag, to)) {
             tma_store_4d(&tmO, stage, h * 64, U.kvh * p.G, U.q0 + t * p.Mq, U.b);
@@ -726,6 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (U.n_tiles > 0) {
         g_tile += U.n_tiles;
         ++qn;
+        if (U.n_tiles >= 2) ++n2;
       }
     }
   }
