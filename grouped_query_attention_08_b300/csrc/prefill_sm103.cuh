@@ -657,22 +657,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           aborted = true;
           break;
         }
-        // Hand-off: S_t(j+1)'s first 64 columns into registers, P_t(j) over
-        // them (bf16 pairs fill exactly 64 columns), then the other 64.
+        // Hand-off: S_t(j+1) into registers, then P_t(j) over its first 64
+        // columns (bf16 pairs fill exactly 64 columns).
         if (j + 1 < n) {
           tmem_ld_32x32b_x32(tS + 0, sv + 0);
           tmem_ld_32x32b_x32(tS + 32, sv + 32);
-          tmem_ld_wait_x32(sv);
-          tmem_ld_wait_x32(sv + 32);
+          tmem_ld_32x32b_x32(tS + 64, sv + 64);
+          tmem_ld_32x32b_x32(tS + 96, sv + 96);
+          tmem_ld_wait_x128(sv);
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_st_32x32b_x16(tS + uint32_t(q) * 16u, pall + q * 16);
-        if (j + 1 < n) {
-          tmem_ld_32x32b_x32(tS + 64, sv + 64);
-          tmem_ld_32x32b_x32(tS + 96, sv + 96);
-          tmem_ld_wait_x32(sv + 64);
-          tmem_ld_wait_x32(sv + 96);
-        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
