@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = U.n_tiles;
         if (n == 0) continue;
         const int qb = int(qn % QB);
-        // QK^T_t of the unit's key tile jj, K from ring stage (g + jj) % S
+        // QK^T_t of the unit's key tile jj (jj = 0, 1), K from ring stage (g + jj) % S
         auto qk = [&](int jj) -> bool {
           const uint32_t it = g + uint32_t(jj);
           const int s = int(it % S);
@@ -459,16 +459,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < n; ++j) {
           const uint32_t it = g + uint32_t(j);
           const int s = int(it % S);
-          ok = mbar_wait(v_full(s), (it / S) & 1, abort_flag, to) && mbar_wait(p_full(tq), it & 1, abort_flag, to);
+          // K of tile j+2 first: loaded long ago, so this wait hides under the P wait
+          const bool more = j + 2 < n;
+          const uint32_t it2 = it + 2u;
+          const int s2 = int(it2 % S);
+          if (more) ok = mbar_wait(k_full(s2), (it2 / S) & 1, abort_flag, to);
+          ok = ok && mbar_wait(v_full(s), (it / S) & 1, abort_flag, to) && mbar_wait(p_full(tq), it & 1, abort_flag, to);
           // the unit's first PV overwrites O_t: the previous epilogue must have read it
           if (ok && j == 0 && qn > 0) ok = mbar_wait(o_free(tq), (qn - 1) & 1, abort_flag, to);
           if (!ok) break;
           tc_fence_after();
           issue_pv(tq, s, j > 0);
+          if (more) {
+            // QK_t(j+2) straight after PV_t(j), which it follows in the tensor core
+            issue_s(tq, qb, s2);
+            umma_commit(s_full(tq));
+          }
           if (j == n - 2) umma_commit(pv_done(tq));   // lets the softmax rescale O_t before the last PV
           if (j == n - 1) umma_commit(o_done(tq));
           umma_commit(v_empty(s));
-          if (j + 2 < n) ok = qk(j + 2);
+          if (more) {
+            umma_commit(k_empty(s2));
+            if (!L::kQInTmem && j + 3 == n) umma_commit(q_empty(qb));   // the unit's last read of Q
+          }
         }
         if (n >= 2) ++n2;
         g += uint32_t(n);
