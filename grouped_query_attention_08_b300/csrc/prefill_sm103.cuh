@@ -459,25 +459,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; ok && j < n; ++j) {
           const uint32_t it = g + uint32_t(j);
           const int s = int(it % S);
-          // K of tile j+2 first: loaded long ago, so this wait hides under the P wait
+          // With a ring of four or more stages K of tile j+2 was loaded long
+          // ago, so its wait goes first and hides under the P wait; with two
+          // stages it shares K(j)'s stage and is loaded just in time, so it is
+          // waited for after PV(j).
+          constexpr bool kEarlyK = S >= 4;
           const bool more = j + 2 < n;
           const uint32_t it2 = it + 2u;
           const int s2 = int(it2 % S);
-          if (more) ok = mbar_wait(k_full(s2), (it2 / S) & 1, abort_flag, to);
+          if (kEarlyK && more) ok = mbar_wait(k_full(s2), (it2 / S) & 1, abort_flag, to);
           ok = ok && mbar_wait(v_full(s), (it / S) & 1, abort_flag, to) && mbar_wait(p_full(tq), it & 1, abort_flag, to);
           // the unit's first PV overwrites O_t: the previous epilogue must have read it
           if (ok && j == 0 && qn > 0) ok = mbar_wait(o_free(tq), (qn - 1) & 1, abort_flag, to);
           if (!ok) break;
           tc_fence_after();
           issue_pv(tq, s, j > 0);
+          // Deep ring: QK_t(j+2) straight after PV_t(j), the release commits
+          // after it.  Two-stage ring: V(j) is released at once (the next V
+          // load waits for it) and K(j+2) is waited for here.
+          if constexpr (!kEarlyK) {
+            if (j == n - 2) umma_commit(pv_done(tq));   // lets the softmax rescale O_t before the last PV
+            if (j == n - 1) umma_commit(o_done(tq));
+            umma_commit(v_empty(s));
+            if (more) {
+              ok = mbar_wait(k_full(s2), (it2 / S) & 1, abort_flag, to);
+              if (!ok) break;
+              tc_fence_after();
+            }
+          }
           if (more) {
-            // QK_t(j+2) straight after PV_t(j), which it follows in the tensor core
+            // QK_t(j+2) follows PV_t(j) in the tensor core (same issuing thread)
             issue_s(tq, qb, s2);
             umma_commit(s_full(tq));
           }
-          if (j == n - 2) umma_commit(pv_done(tq));   // lets the softmax rescale O_t before the last PV
-          if (j == n - 1) umma_commit(o_done(tq));
-          umma_commit(v_empty(s));
+          if constexpr (kEarlyK) {
+            if (j == n - 2) umma_commit(pv_done(tq));
+            if (j == n - 1) umma_commit(o_done(tq));
+            umma_commit(v_empty(s));
+          }
           if (more) {
             umma_commit(k_empty(s2));
             if (!L::kQInTmem && j + 3 == n) umma_commit(q_empty(qb));   // the unit's last read of Q
