@@ -254,14 +254,26 @@ def time_prefill_workload(gqa, name, device, flush, reps=10, warmup=3):
     w = inputs.WORKLOADS[name]
     inp = inputs.make_workload(w)
     d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    lens = None if inp["seqlens_k"] is None else inp["seqlens_k"].tolist()
-    flops = roofline.prefill_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal, lens)
     out = torch.empty_like(d["q"])
-    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=device)
+    if isinstance(w, inputs.VarlenWorkload):
+        # packed sequences: only real (query, key) pairs are work
+        lq = (inp["cu_seqlens_q"][1:] - inp["cu_seqlens_q"][:-1]).tolist()
+        lk = (inp["cu_seqlens_k"][1:] - inp["cu_seqlens_k"][:-1]).tolist()
+        flops = roofline.varlen_flops(w.Hq, w.D, lq, lk, w.causal)
+        lse = torch.empty((w.Hq, d["q"].shape[0]), dtype=torch.float32, device=device)
 
-    def call():
-        gqa.gqa_fwd(d["q"], d["k"], d["v"], causal=w.causal, seqlens_k=d["seqlens_k"], scale=w.scale,
-                    out=out, lse=lse)
+        def call():
+            gqa.gqa_fwd_varlen(d["q"], d["k"], d["v"], d["cu_seqlens_q"], d["cu_seqlens_k"],
+                               max_seqlen_q=d["max_seqlen_q"], max_seqlen_k=d["max_seqlen_k"], causal=w.causal,
+                               scale=w.scale, out=out, lse=lse)
+    else:
+        lens = None if inp["seqlens_k"] is None else inp["seqlens_k"].tolist()
+        flops = roofline.prefill_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal, lens)
+        lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=device)
+
+        def call():
+            gqa.gqa_fwd(d["q"], d["k"], d["v"], causal=w.causal, seqlens_k=d["seqlens_k"], scale=w.scale,
+                        out=out, lse=lse)
 
     for _ in range(warmup):
         flush.fill_(1)
@@ -279,6 +291,9 @@ def time_prefill_workload(gqa, name, device, flush, reps=10, warmup=3):
 
 
 def _workload_name(w):
+    if isinstance(w, inputs.VarlenWorkload):
+        return "%s packed prefill B%d Hq%d Hkv%d D%d %s lengths U[%d,%d] (queries = keys), no padding" % (
+            w.name, w.B, w.Hq, w.Hkv, w.D, "causal" if w.causal else "non-causal", w.lens[0], w.lens[1])
     lens = "full" if w.lens is None else "U[%d,%d]" % w.lens
     return "%s prefill B%d Hq%d Hkv%d Sq%d Sk%d D%d %s keys %s" % (
         w.name, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, "causal" if w.causal else "non-causal", lens)
@@ -439,7 +454,7 @@ def main():
     others = {}
     if not args.no_other_workloads:
         del P, pin, out_p, lse_p
-        for name in ("bert_base", "bert_large_long", "causal_long"):
+        for name in ("bert_base", "bert_large_long", "causal_long", "bert_base_varlen"):
             if name == args.prefill:
                 others[name] = {"tflops": value / ws, "ms": pre_avg * 1e3}
                 continue

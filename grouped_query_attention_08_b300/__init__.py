@@ -60,6 +60,9 @@ def load_library():
         vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.gqa_fwd.restype = i32
         lib.gqa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, i32, vp]
+        lib.gqa_fwd_varlen.restype = i32
+        lib.gqa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
+                                       f32, i32, i32, vp]
         lib.gqa_decode.restype = i32
         lib.gqa_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, vp, sz, vp]
         lib.gqa_decode_num_splits.restype = i32
@@ -153,6 +156,51 @@ def gqa_fwd(q, k, v, *, causal=False, seqlens_k=None, scale=None, out=None, lse=
                                 _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_fwd")
+    return out, lse
+
+
+def gqa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q=None, max_seqlen_k=None,
+                   causal=False, scale=None, out=None, lse=None, return_lse=True, stream=None):
+    """GQA attention over sequences packed without padding.
+
+    q [total_q,Hq,D], k/v [total_k,Hkv,D] (bf16 or fp32, CUDA); cu_seqlens_q/k int32
+    CUDA tensors [B+1] of row offsets.  Returns (out [total_q,Hq,D], lse [Hq,total_q]
+    fp32 or None).  ``max_seqlen_q/k`` bound the sequence lengths; when None they are
+    read from the offsets (a device-to-host copy that synchronises the stream).
+    """
+    torch = _torch()
+    if q.dim() != 3 or k.dim() != 3 or v.dim() != 3:
+        raise ValueError("q, k, v must be 3-D [total, H, D]")
+    total_q, Hq, D = q.shape
+    total_k, Hkv, Dk = k.shape
+    if Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between q, k and v")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    code = _dtype_code(q)
+    for name, cu in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_k", cu_seqlens_k)):
+        if cu.dtype != torch.int32 or cu.dim() != 1 or cu.shape[0] < 2:
+            raise ValueError("%s must be int32 [B+1]" % name)
+    if cu_seqlens_k.shape != cu_seqlens_q.shape:
+        raise ValueError("cu_seqlens_q and cu_seqlens_k must both be [B+1]")
+    B = cu_seqlens_q.shape[0] - 1
+    if max_seqlen_q is None:
+        max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item())
+    if max_seqlen_k is None:
+        max_seqlen_k = int((cu_seqlens_k[1:] - cu_seqlens_k[:-1]).max().item())
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((Hq, total_q), dtype=torch.float32, device=q.device)
+    dev = _check_cuda(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = load_library().gqa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                                       _ptr(cu_seqlens_k), B, Hq, Hkv, max(int(max_seqlen_q), 1),
+                                       max(int(max_seqlen_k), 1), total_q, total_k, D, float(scale),
+                                       int(bool(causal)), code, _stream(dev, stream))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_fwd_varlen")
     return out, lse
 
 

@@ -27,7 +27,14 @@ struct Params {
   float* lse;          // [B, Hq, Sq] or nullptr (nsplit == 1)
   float* part_o;       // [B*Hq*Sq rows, nsplit, D] (nsplit > 1)
   float* part_lse;     // [rows, nsplit]
-  const int* seqlens;  // [B] or nullptr
+  const int* seqlens;  // [B] or nullptr (dense layout)
+  // Packed layout when cu_q != nullptr: q/out [total_q, Hq, D], k/v
+  // [total_k, Hkv, D], lse [Hq, total_q]; sequence b owns query rows
+  // [cu_q[b], cu_q[b+1]) and key rows [cu_k[b], cu_k[b+1]); Sq / Sk are the
+  // largest sequence lengths.
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
   long long q_sb, q_ss, q_sh;   // element strides of q/out: batch, token, head
   long long k_sb, k_ss, k_sh;   // element strides of k/v: batch, key, kv head
   int B, Hq, Hkv, G, Sq, Sk, D, causal;
@@ -39,37 +46,64 @@ struct Params {
 __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const Params p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const long long row = (long long)blockIdx.x * kWarps + warp;   // (b * Hq + h) * Sq + i
-  const long long nrows = (long long)p.B * p.Hq * p.Sq;
+  // dense: row = (b * Hq + h) * Sq + i;  packed: row = h * total_q + packed row
+  const long long row = (long long)blockIdx.x * kWarps + warp;
+  const long long nrows = p.cu_q ? (long long)p.Hq * p.total_q : (long long)p.B * p.Hq * p.Sq;
   if (row >= nrows) return;
   const int split = blockIdx.y;
-  const int i = int(row % p.Sq);
-  const int h = int((row / p.Sq) % p.Hq);
-  const int b = int(row / ((long long)p.Sq * p.Hq));
+  int i, h, b, Lb, diag;
+  long long q_off, k_off;       // element offsets of the row's query and of the sequence's key 0
+  bool ok = true;
+  if (p.cu_q) {
+    h = int(row / p.total_q);
+    const int gi = int(row % p.total_q);
+    int lo = 0, hi = p.B;     // last b with cu_q[b] <= gi
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.cu_q[mid] <= gi) lo = mid; else hi = mid;
+    }
+    if (gi >= p.cu_q[p.B]) return;   // a packed row after the last sequence: not written
+    b = lo;
+    const int qs = p.cu_q[b], qe = p.cu_q[b + 1], ks = p.cu_k[b], ke = p.cu_k[b + 1];
+    i = gi - qs;
+    Lb = ke - ks;
+    const int Lq = qe - qs;
+    ok = qs >= 0 && qs <= gi && gi < qe && Lq <= p.Sq && ks >= 0 && Lb >= 0 && Lb <= p.len_cap && ke <= p.total_k;
+    diag = Lb - Lq;
+    q_off = (long long)gi * p.q_ss + (long long)h * p.q_sh;
+    k_off = (long long)ks * p.k_ss;
+  } else {
+    i = int(row % p.Sq);
+    h = int((row / p.Sq) % p.Hq);
+    b = int(row / ((long long)p.Sq * p.Hq));
+    Lb = p.seqlens ? p.seqlens[b] : p.Sk;
+    ok = Lb >= 0 && Lb <= p.len_cap;
+    diag = p.Sk - p.Sq;
+    q_off = b * p.q_sb + (long long)i * p.q_ss + (long long)h * p.q_sh;
+    k_off = b * p.k_sb;
+  }
   const int kvh = h / p.G;
-
-  int Lb = p.seqlens ? p.seqlens[b] : p.Sk;
-  if (Lb < 0 || Lb > p.len_cap) {
-    if (lane == 0 && i == 0 && h == 0 && split == 0) raise_error(kErrBounds);
+  if (!ok) {
+    if (lane == 0 && split == 0 && (p.cu_q || (i == 0 && h == 0))) raise_error(kErrBounds);
     Lb = 0;
   }
   int lim = Lb;
-  if (p.causal) lim = min(lim, i + p.Sk - p.Sq + 1);
+  if (p.causal) lim = min(lim, i + diag + 1);
   lim = max(lim, 0);
   const int j0 = split * p.split_len;
   const int j1 = min(lim, j0 + p.split_len);
 
   constexpr int E = kMaxD / 32;
   float qv[E], ov[E];
-  const float* qrow = p.q + b * p.q_sb + (long long)i * p.q_ss + (long long)h * p.q_sh;
+  const float* qrow = p.q + q_off;
 #pragma unroll
   for (int e = 0; e < E; ++e) {
     const int d = lane + 32 * e;
     qv[e] = d < p.D ? qrow[d] : 0.f;
     ov[e] = 0.f;
   }
-  const float* kb = p.k + b * p.k_sb + (long long)kvh * p.k_sh;
-  const float* vb = p.v + b * p.k_sb + (long long)kvh * p.k_sh;
+  const float* kb = p.k + k_off + (long long)kvh * p.k_sh;
+  const float* vb = p.v + k_off + (long long)kvh * p.k_sh;
   float m = -INFINITY, l = 0.f;
   for (int j = j0; j < j1; ++j) {
     const float* kr = kb + (long long)j * p.k_ss;
@@ -97,7 +131,7 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const Params p) 
   const float inv = l > 0.f ? 1.f / l : 0.f;
   const float lse = l > 0.f ? m + logf(l) : -INFINITY;
   if (p.nsplit == 1) {
-    float* orow = p.out + b * p.q_sb + (long long)i * p.q_ss + (long long)h * p.q_sh;
+    float* orow = p.out + q_off;
 #pragma unroll
     for (int e = 0; e < E; ++e) {
       const int d = lane + 32 * e;

@@ -118,21 +118,28 @@ bool prefill_smem_attr_set(int dev) {
   namespace pf = gqa::prefill;
   static bool done[kMaxDevices] = {false};
   if (dev >= 0 && dev < kMaxDevices && done[dev]) return true;
-  const void* fn = reinterpret_cast<const void*>(pf::prefill_kernel<D>);
   const int smem = int(pf::Layout<D>::kSmemAlloc);
-  cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return false;
   static_assert(2 * 128 * pf::kSoftmaxRegs + 128 * pf::kOtherRegs <= pf::kThreads * pf::kLaunchRegs,
                 "register split exceeds the launch budget");
-  if (fa.numRegs != pf::kLaunchRegs) return false;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+  // both layouts: dense and packed
+  for (const void* fn : {reinterpret_cast<const void*>(pf::prefill_kernel<D, false>),
+                         reinterpret_cast<const void*>(pf::prefill_kernel<D, true>)}) {
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return false;
+    if (fa.numRegs != pf::kLaunchRegs) return false;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) return false;
+  }
   if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
   return true;
 }
 
+// Dense layout (cu_q == nullptr): q/out [B, Sq, Hq, D], k/v [B, Sk, Hkv, D].
+// Packed layout: q/out [total_q, Hq, D], k/v [total_k, Hkv, D], sequence b at
+// rows cu_q[b].. / cu_k[b].., Sq / Sk = the largest sequence lengths.
 template <int D>
 int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
-                        int Sq, int Sk, float scale, int causal, const int* seqlens_k, cudaStream_t stream) {
+                        int Sq, int Sk, float scale, int causal, const int* seqlens_k, const int* cu_q,
+                        const int* cu_k, int total_q, int total_k, cudaStream_t stream) {
   namespace pf = gqa::prefill;
   const int G = Hq / Hkv;
   const int Mq = pf::kBM / G;
@@ -143,14 +150,25 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   // use allow no more), each looping over work units
   const long long grid = std::min<long long>(n_units, num_sms(current_device()));
   CUtensorMap tmQ, tmK, tmV, tmO;
-  if (!encode_4d_bf16(&tmQ, q, D, Hq, Sq, B, 64, G, Mq, 1) || !encode_4d_bf16(&tmK, k, D, Hkv, Sk, B, 64, 1, 128, 1) ||
-      !encode_4d_bf16(&tmV, v, D, Hkv, Sk, B, 64, 1, 128, 1) || !encode_4d_bf16(&tmO, out, D, Hq, Sq, B, 64, G, Mq, 1))
+  // packed: the maps see one batch entry of total_q / total_k rows
+  const uint64_t mq_rows = cu_q ? uint64_t(total_q) : uint64_t(Sq);
+  const uint64_t mk_rows = cu_q ? uint64_t(total_k) : uint64_t(Sk);
+  const uint64_t m_batch = cu_q ? 1u : uint64_t(B);
+  if (!encode_4d_bf16(&tmQ, q, D, Hq, mq_rows, m_batch, 64, G, Mq, 1) ||
+      !encode_4d_bf16(&tmK, k, D, Hkv, mk_rows, m_batch, 64, 1, 128, 1) ||
+      !encode_4d_bf16(&tmV, v, D, Hkv, mk_rows, m_batch, 64, 1, 128, 1) ||
+      !encode_4d_bf16(&tmO, out, D, Hq, mq_rows, m_batch, 64, G, Mq, 1))
     return GQA_ERR_CUDA;
   if (!prefill_smem_attr_set<D>(current_device())) return GQA_ERR_CUDA;
-  pf::Params p;
+  pf::Params p{};
   p.out = static_cast<__nv_bfloat16*>(out);
   p.lse = lse;
-  p.seqlens = seqlens_k;
+  p.seqlens = cu_q ? nullptr : seqlens_k;
+  p.cu_q = cu_q;
+  p.cu_k = cu_q ? cu_k : nullptr;
+  p.total_q = total_q;
+  p.total_k = total_k;
+  p.lse_stride = cu_q ? total_q : Sq;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -165,8 +183,12 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.timeout_ns = wait_timeout_ns();
-  pf::prefill_kernel<D><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(tmQ, tmK, tmV, tmO,
-                                                                                          p);
+  if (cu_q)
+    pf::prefill_kernel<D, true><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(tmQ, tmK, tmV,
+                                                                                                 tmO, p);
+  else
+    pf::prefill_kernel<D, false><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(tmQ, tmK, tmV,
+                                                                                                  tmO, p);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
@@ -193,7 +215,7 @@ bool decode_smem_attr_set(int dev) {
 }
 
 int launch_f32(const gqa::f32::Params& p, cudaStream_t stream) {
-  const long long rows = (long long)p.B * p.Hq * p.Sq;
+  const long long rows = p.cu_q ? (long long)p.Hq * p.total_q : (long long)p.B * p.Hq * p.Sq;
   const long long gx = (rows + gqa::f32::kWarps - 1) / gqa::f32::kWarps;
   if (gx > 0x7fffffffLL || p.nsplit > 65535) return GQA_ERR_UNSUPPORTED;
   gqa::f32::attention_kernel<<<dim3(unsigned(gx), unsigned(p.nsplit)), gqa::f32::kWarps * 32, 0, stream>>>(p);
@@ -265,8 +287,10 @@ int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, 
     if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
     if (Hq / Hkv > gqa::prefill::kBM) return GQA_ERR_UNSUPPORTED;
     if ((long long)Hq * D * Sq * B > (1LL << 40)) return GQA_ERR_UNSUPPORTED;
-    return D == 64 ? launch_prefill_bf16<64>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k, st)
-                   : launch_prefill_bf16<128>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k, st);
+    return D == 64 ? launch_prefill_bf16<64>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k,
+                                             nullptr, nullptr, 0, 0, st)
+                   : launch_prefill_bf16<128>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k,
+                                              nullptr, nullptr, 0, 0, st);
   }
   if (dtype == GQA_DTYPE_FP32) {
     if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4)) return GQA_ERR_INVALID_ARG;
@@ -296,6 +320,63 @@ int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, 
     p.nsplit = 1;
     p.split_len = Sk;
     p.len_cap = Sk;
+    return launch_f32(p, st);
+  }
+  return GQA_ERR_INVALID_ARG;
+}
+
+int gqa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float* lse, const int* cu_seqlens_q,
+                   const int* cu_seqlens_k, int B, int Hq, int Hkv, int max_seqlen_q, int max_seqlen_k, int total_q,
+                   int total_k, int D, float scale, int causal, int dtype, void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_seqlen_q <= 0 || max_seqlen_k <= 0 || total_q <= 0 ||
+      total_k <= 0)
+    return GQA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return GQA_ERR_INVALID_ARG;
+  if (!aligned(cu_seqlens_q, 4) || !aligned(cu_seqlens_k, 4) || (lse && !aligned(lse, 4))) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == GQA_DTYPE_BF16) {
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return GQA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+    if (Hq / Hkv > gqa::prefill::kBM) return GQA_ERR_UNSUPPORTED;
+    if ((long long)Hq * D * total_q > (1LL << 40) || (long long)Hkv * D * total_k > (1LL << 40))
+      return GQA_ERR_UNSUPPORTED;
+    return D == 64 ? launch_prefill_bf16<64>(q, k, v, out, lse, B, Hq, Hkv, max_seqlen_q, max_seqlen_k, scale,
+                                             causal, nullptr, cu_seqlens_q, cu_seqlens_k, total_q, total_k, st)
+                   : launch_prefill_bf16<128>(q, k, v, out, lse, B, Hq, Hkv, max_seqlen_q, max_seqlen_k, scale,
+                                              causal, nullptr, cu_seqlens_q, cu_seqlens_k, total_q, total_k, st);
+  }
+  if (dtype == GQA_DTYPE_FP32) {
+    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4)) return GQA_ERR_INVALID_ARG;
+    if (D > gqa::f32::kMaxD) return GQA_ERR_UNSUPPORTED;
+    gqa::f32::Params p{};
+    p.q = static_cast<const float*>(q);
+    p.k = static_cast<const float*>(k);
+    p.v = static_cast<const float*>(v);
+    p.out = static_cast<float*>(out);
+    p.lse = lse;
+    p.cu_q = cu_seqlens_q;
+    p.cu_k = cu_seqlens_k;
+    p.total_q = total_q;
+    p.total_k = total_k;
+    p.q_ss = (long long)Hq * D;
+    p.q_sh = D;
+    p.k_ss = (long long)Hkv * D;
+    p.k_sh = D;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.Sq = max_seqlen_q;
+    p.Sk = max_seqlen_k;
+    p.D = D;
+    p.causal = causal;
+    p.scale = scale;
+    p.nsplit = 1;
+    p.split_len = max_seqlen_k;
+    p.len_cap = max_seqlen_k;
     return launch_f32(p, st);
   }
   return GQA_ERR_INVALID_ARG;

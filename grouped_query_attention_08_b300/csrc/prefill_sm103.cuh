@@ -104,7 +104,7 @@ struct Layout {
   static constexpr int kNumBars = 2 * kQBufs + 4 * kStages + 4 * kNQT + 1 + 2 * kNQT + 2 * kUQ + 2 * kNQT + 1;
   // unit queue: kUQ entries of (unit index, key length)
   static constexpr uint32_t kOffUQ = kOffBar + 8u * kNumBars;
-  static constexpr uint32_t kOffTmemSlot = kOffUQ + 8u * kUQ;
+  static constexpr uint32_t kOffTmemSlot = kOffUQ + 32u * kUQ;
   static constexpr uint32_t kOffAbort = kOffTmemSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
   static constexpr uint32_t kSmemAlloc = kBytes + 1024u;    // slack to align the base to 1024 B
@@ -121,9 +121,17 @@ struct Layout {
 };
 
 struct Params {
-  __nv_bfloat16* out;     // [B, Sq, Hq, D]
-  float* lse;             // [B, Hq, Sq] or nullptr
-  const int* seqlens;     // [B] or nullptr
+  __nv_bfloat16* out;     // [B, Sq, Hq, D]; packed: [total_q, Hq, D]
+  float* lse;             // [B, Hq, Sq]; packed: [Hq, total_q]; or nullptr
+  const int* seqlens;     // [B] or nullptr (dense layout only)
+  // Packed (variable-length) layout when cu_q != nullptr: sequence b owns
+  // query rows [cu_q[b], cu_q[b+1]) and key rows [cu_k[b], cu_k[b+1]); the
+  // tensor maps then see one batch entry of total_q / total_k rows, and Sq /
+  // Sk are the largest sequence lengths.
+  const int* cu_q;
+  const int* cu_k;
+  int total_q, total_k;
+  int lse_stride;         // Sq (dense) or total_q (packed)
   int B, Hq, Hkv, G, Sq, Sk;
   int Mq;                 // tokens per Q tile (G * Mq <= 128)
   int n_qblk;             // ceil(Sq / (kNQT * Mq))
@@ -139,7 +147,18 @@ struct Params {
 
 struct Unit {
   int b, kvh, q0, Lb, n_tiles;
+  int Lq;                  // query rows of the sequence (Sq when dense)
+  int qbase, kbase;        // first packed row of the sequence (0 when dense)
+  int tb;                  // batch coordinate of the tensor maps (b, or 0 when packed)
+  int diag;                // causal: query row i sees keys j <= i + diag
+  bool has_rows;           // the unit holds at least one query row
   bool bad_len;
+};
+
+// Lengths and packed row offsets of a work unit's sequence, read by the TMA
+// warp one unit ahead and passed on through the unit queue.
+struct SeqInfo {
+  int Lk, Lq, qbase, kbase;
 };
 
 // Position of work unit u = qidx * (B * Hkv) + b * Hkv + kvh.
@@ -158,11 +177,28 @@ DEVI UnitPos upos_of(const Params& p, int u) {
 }
 
 // Key length of the unit's batch entry.
-DEVI int unit_len(const Params& p, const UnitPos& x) {
-  if (!p.seqlens) return p.Sk;
+DEVI int ldg_nc_i32(const int* a) {
   int v;
-  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p.seqlens + x.b));
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(a));
   return v;
+}
+template <bool kPacked>
+DEVI SeqInfo unit_seq(const Params& p, const UnitPos& x) {
+  SeqInfo q;
+  if constexpr (kPacked) {
+    const int q0 = ldg_nc_i32(p.cu_q + x.b), q1 = ldg_nc_i32(p.cu_q + x.b + 1);
+    const int k0 = ldg_nc_i32(p.cu_k + x.b), k1 = ldg_nc_i32(p.cu_k + x.b + 1);
+    q.Lq = q1 - q0;
+    q.Lk = k1 - k0;
+    q.qbase = q0;
+    q.kbase = k0;
+  } else {
+    q.Lk = p.seqlens ? ldg_nc_i32(p.seqlens + x.b) : p.Sk;
+    q.Lq = p.Sq;
+    q.qbase = 0;
+    q.kbase = 0;
+  }
+  return q;
 }
 
 // Claims the next work unit of this launch (returns gridDim.x + a running
@@ -176,24 +212,41 @@ DEVI int claim_unit(const Params& p) {
 
 // Work unit -> (b, kvh, first token, key length, number of key tiles); len is
 // unit_len of the same unit.
-DEVI Unit unit_info(const Params& p, const UnitPos& x, int len) {
+template <bool kPacked>
+DEVI Unit unit_info(const Params& p, const UnitPos& x, const SeqInfo& sq) {
   Unit U;
   const int qblk = p.causal ? p.n_qblk - 1 - x.qidx : x.qidx;   // causal: longest units first
   U.b = x.b;
   U.kvh = x.kvh;
   U.q0 = qblk * kNQT * p.Mq;
-  int Lb = len;
-  U.bad_len = (Lb < 0 || Lb > p.Sk);
-  if (U.bad_len) Lb = 0;
+  int Lb = sq.Lk, Lq = kPacked ? sq.Lq : p.Sq;
+  U.bad_len = (Lb < 0 || Lb > p.Sk || Lq < 0 || Lq > p.Sq);
+  if (kPacked)
+    U.bad_len = U.bad_len || sq.qbase < 0 || sq.kbase < 0 || sq.qbase > p.total_q - Lq ||
+                sq.kbase > p.total_k - Lb;
+  if (U.bad_len) {
+    // a dense unit still writes zeros for its rows; a packed one cannot
+    // place its rows and writes nothing
+    Lb = 0;
+    if (kPacked) Lq = 0;
+  }
   U.Lb = Lb;
-  const int q_last = min(U.q0 + kNQT * p.Mq, p.Sq) - 1;
+  U.Lq = Lq;
+  U.qbase = kPacked ? sq.qbase : 0;
+  U.kbase = kPacked ? sq.kbase : 0;
+  U.tb = kPacked ? 0 : x.b;
+  U.has_rows = U.q0 < Lq;
+  // bottom-right aligned diagonal: of the padded sizes (dense) or of the
+  // sequence's own lengths (packed)
+  U.diag = kPacked ? Lb - Lq : p.Sk - p.Sq;
+  const int q_last = min(U.q0 + kNQT * p.Mq, Lq) - 1;
   int kmax = Lb;
-  if (p.causal) kmax = min(kmax, q_last + p.Sk - p.Sq + 1);
-  U.n_tiles = kmax > 0 ? (kmax + kBN - 1) / kBN : 0;
+  if (p.causal) kmax = min(kmax, q_last + U.diag + 1);
+  U.n_tiles = (U.has_rows && kmax > 0) ? (kmax + kBN - 1) / kBN : 0;
   return U;
 }
 
-template <int D>
+template <int D, bool kPacked>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -232,18 +285,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffTmemSlot);
   const uint64_t to = p.timeout_ns;
-  volatile int* uq = reinterpret_cast<volatile int*>(sbase + L::kOffUQ);   // [kUQ][2]: unit, key length
+  // [kUQ][8]: unit, then the SeqInfo fields Lk, Lq, qbase, kbase
+  volatile int* uq = reinterpret_cast<volatile int*>(sbase + L::kOffUQ);
   // Consumer side of the unit queue: entry k's (unit, key length), or
   // n_units when the wait gave up.  A whole warp (softmax) releases the
   // entry with one arrival once every lane has read it; a single thread
   // (MMA issuer) arrives itself.
-  auto next_unit = [&](uint32_t k, int& len, bool& ok, bool whole_warp) -> int {
+  auto next_unit = [&](uint32_t k, SeqInfo& sq, bool& ok, bool whole_warp) -> int {
     const int i = int(k % kUQ);
     ok = mbar_wait(uq_full(i), (k / kUQ) & 1, abort_flag, p.timeout_ns);
     int u = p.n_units;
     if (ok) {
-      u = uq[2 * i];
-      len = uq[2 * i + 1];
+      u = uq[8 * i];
+      sq.Lk = uq[8 * i + 1];
+      if constexpr (kPacked) {
+        sq.Lq = uq[8 * i + 2];
+        sq.qbase = uq[8 * i + 3];
+        sq.kbase = uq[8 * i + 4];
+      }
     }
     if (whole_warp) {
       __syncwarp();
@@ -322,13 +381,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = mbar_wait(uq_empty(i), ((k / kUQ) & 1) ^ 1, abort_flag, to);
         if (!ok) break;
         const UnitPos x = upos_of(p, u < p.n_units ? u : 0);
-        const int len = (u < p.n_units) ? unit_len(p, x) : 0;
+        SeqInfo sq{0, 0, 0, 0};
+        if (u < p.n_units) sq = unit_seq<kPacked>(p, x);
         if (u < p.n_units) u_next = claim_unit(p);
-        uq[2 * i] = u;
-        uq[2 * i + 1] = len;
+        uq[8 * i] = u;
+        uq[8 * i + 1] = sq.Lk;
+        uq[8 * i + 2] = sq.Lq;
+        uq[8 * i + 3] = sq.qbase;
+        uq[8 * i + 4] = sq.kbase;
         mbar_arrive(uq_full(i));        // release: the entry is visible to the consumers
         if (u >= p.n_units) break;
-        const Unit U = unit_info(p, x, len);
+        const Unit U = unit_info<kPacked>(p, x, sq);
         if (U.bad_len) raise_error(kErrBounds);
         if (U.n_tiles == 0) continue;
         const int qb = int(qn % QB);
@@ -338,7 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; t < kNQT; ++t)
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_4d(base + L::kOffQ + qb * L::kQSetBytes + t * L::kTileBytes + h * L::kHalfBytes, &tmQ,
-                        q_full(qb), h * 64, U.kvh * p.G, U.q0 + t * p.Mq, U.b);
+                        q_full(qb), h * 64, U.kvh * p.G, U.qbase + U.q0 + t * p.Mq, U.tb);
         ++qn;
         for (int j = 0; j < U.n_tiles; ++j) {
           const int s = int(kv_it % S);
@@ -348,7 +411,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(k_full(s), L::kTileBytes);
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_4d(base + L::kOffK + s * L::kTileBytes + h * L::kHalfBytes, &tmK, k_full(s), h * 64,
-                        U.kvh, j * kBN, U.b);
+                        U.kvh, U.kbase + j * kBN, U.tb);
           ok = mbar_wait(v_empty(s), ph ^ 1, abort_flag, to);
           if (!ok) {
             k_only = true;     // K of ring position kv_it is in flight, V is not
@@ -357,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(v_full(s), L::kTileBytes);
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_4d(base + L::kOffV + s * L::kTileBytes + h * L::kHalfBytes, &tmV, v_full(s), h * 64,
-                        U.kvh, j * kBN, U.b);
+                        U.kvh, U.kbase + j * kBN, U.tb);
           ++kv_it;
         }
       }
@@ -427,10 +490,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t n2 = 0;          // units with two or more key tiles so far (s_free / pv_done phases)
       bool ok = true;
       for (uint32_t k = 0; ok; ++k) {
-        int len = 0;
-        const int u = next_unit(k, len, ok, false);
+        SeqInfo sq;
+        const int u = next_unit(k, sq, ok, false);
         if (!ok || u >= p.n_units) break;
-        const Unit U = unit_info(p, upos_of(p, u), len);
+        const Unit U = unit_info<kPacked>(p, upos_of(p, u), sq);
         const int n = U.n_tiles;
         if (n == 0) continue;
         const int qb = int(qn % QB);
@@ -535,21 +598,21 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int r_tok = r / p.G;   // token of this row within the Q tile
     for (uint32_t k = 0; !aborted; ++k) {
-      int len = 0;
+      SeqInfo sq;
       bool qok;
-      const int u = next_unit(k, len, qok, true);
+      const int u = next_unit(k, sq, qok, true);
       if (!__all_sync(0xffffffffu, qok)) {
         aborted = true;
         break;
       }
       if (u >= p.n_units) break;
-      const Unit U = unit_info(p, upos_of(p, u), len);
+      const Unit U = unit_info<kPacked>(p, upos_of(p, u), sq);
       const int token = U.q0 + t * p.Mq + r_tok;
-      const bool row_ok = (r < rows_per_tile) && (token < p.Sq);
+      const bool row_ok = (r < rows_per_tile) && (token < U.Lq);
       int limit = 0;
       if (row_ok) {
         limit = U.Lb;
-        if (p.causal) limit = min(limit, token + p.Sk - p.Sq + 1);
+        if (p.causal) limit = min(limit, token + U.diag + 1);
         limit = max(limit, 0);
       }
       float m = -INFINITY;
@@ -731,7 +794,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < D; ++i) o[i] = 0u;
       }
       const float inv_l = (l > 0.f && have_o) ? 1.f / l : 0.f;
-      if (!aborted) {
+      // A packed Q tile that runs past its sequence (its last rows belong to
+      // the next sequence) is written row by row; every other tile goes out
+      // through shared memory and one TMA store.
+      const bool tile_full = !kPacked || (U.q0 + (t + 1) * p.Mq <= U.Lq);
+      if (!aborted && U.has_rows && !tile_full) {
+        if (row_ok) {
+          __nv_bfloat16* orow =
+              p.out + ((size_t(U.qbase) + size_t(token)) * p.Hq + size_t(U.kvh) * p.G + g) * D;
+#pragma unroll
+          for (int c8 = 0; c8 < D / 8; ++c8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(o[8 * c8 + 0]) * inv_l, __uint_as_float(o[8 * c8 + 1]) * inv_l);
+            w.y = pack_bf16x2(__uint_as_float(o[8 * c8 + 2]) * inv_l, __uint_as_float(o[8 * c8 + 3]) * inv_l);
+            w.z = pack_bf16x2(__uint_as_float(o[8 * c8 + 4]) * inv_l, __uint_as_float(o[8 * c8 + 5]) * inv_l);
+            w.w = pack_bf16x2(__uint_as_float(o[8 * c8 + 6]) * inv_l, __uint_as_float(o[8 * c8 + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(orow + 8 * c8) = w;
+          }
+        }
+      } else if (!aborted && U.has_rows) {
         // Normalised bf16 rows go to a staging block in shared memory, 64
         // columns at a time, and one thread writes each block to global memory
         // with a TMA store (rows of tokens past Sq fall outside the tensor and
@@ -769,14 +850,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(stg_full(t));
           }
           if (leader && ok && mbar_wait(stg_full(t), ph, abort_flag, to)) {
-            tma_store_4d(&tmO, stage, h * 64, U.kvh * p.G, U.q0 + t * p.Mq, U.b);
+            tma_store_4d(&tmO, stage, h * 64, U.kvh * p.G, U.qbase + U.q0 + t * p.Mq, U.tb);
             bulk_commit_group();
           }
         }
-        if (row_ok && p.lse) {
-          const float lse = (l > 0.f && have_o) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
-          p.lse[(size_t(U.b) * p.Hq + size_t(U.kvh) * p.G + g) * p.Sq + token] = lse;
-        }
+      }
+      if (!aborted && row_ok && p.lse) {
+        const float lse = (l > 0.f && have_o) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        p.lse[(size_t(U.tb) * p.Hq + size_t(U.kvh) * p.G + g) * size_t(p.lse_stride) + size_t(U.qbase) + token] =
+            lse;
       }
       if (U.n_tiles > 0) {
         g_tile += U.n_tiles;

@@ -10,6 +10,11 @@ round-to-nearest-even for bf16 workloads; lengths are ``randint(lo, hi+1)``.
 The workloads stand in for the pages' BERT-base seq-1024 encoder, a
 BERT-large long-document encoder, a Llama-style 64/8-head decode step and a
 long causal prefill; no dataset is used.
+
+Packed (variable-length) workloads draw the per-sequence lengths first
+(``randint(lo, hi+1)``, queries and keys sharing a length for
+self-attention), then Q [total_q,Hq,D], K and V [total_k,Hkv,D] in that
+order, cast as above; sequences are packed back to back in index order.
 """
 from __future__ import annotations
 
@@ -56,6 +61,23 @@ class DecodeWorkload:
         return 1.0 / math.sqrt(self.D)
 
 
+@dataclasses.dataclass(frozen=True)
+class VarlenWorkload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    D: int
+    causal: bool
+    lens: Tuple[int, int]            # sequence lengths ~ U[lo, hi] (queries = keys)
+    dtype: str
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+
 WORKLOADS = {
     # tiny fp32 check case: B=1 Hq=4 Hkv=2 S=64 D=64, no padding
     "tiny": PrefillWorkload("tiny", 1, 4, 2, 64, 64, 64, False, None, "fp32", 0),
@@ -71,6 +93,9 @@ WORKLOADS = {
     "llama_decode_small": DecodeWorkload("llama_decode_small", 16, 64, 8, 128, 8192, (1024, 8192), "bf16", 3),
     # long causal prefill, D=128
     "causal_long": PrefillWorkload("causal_long", 4, 32, 8, 8192, 8192, 128, True, None, "bf16", 4),
+    # bert_base's batch packed without padding: each sequence's query and key
+    # length ~ U[512,1024]
+    "bert_base_varlen": VarlenWorkload("bert_base_varlen", 32, 12, 3, 64, False, (512, 1024), "bf16", 1),
 }
 
 
@@ -115,6 +140,36 @@ def make_decode(B, Hq, Hkv, D, Smax, *, seed=0, lens=(1, None), dtype="bf16"):
                 cache_seqlens=seqlens.to(torch.int32))
 
 
+def make_varlen(B, Hq, Hkv, D, *, seed=0, lens=(1, 16), lens_k=None, dtype="bf16"):
+    """Packed sequences: dict(q [total_q,Hq,D], k, v [total_k,Hkv,D], cu_seqlens_q,
+    cu_seqlens_k int32 [B+1], max_seqlen_q, max_seqlen_k) on the CPU.
+
+    ``lens`` = (lo, hi) tuple draws one length per sequence, used for queries
+    and keys alike; ``lens_k`` = (lo, hi) draws separate key lengths after
+    them.  A list instead of a tuple gives the lengths explicitly.
+    """
+    g = torch.Generator("cpu").manual_seed(int(seed))
+
+    def draw(spec):
+        if isinstance(spec, list):          # explicit lengths
+            if len(spec) != B:
+                raise ValueError("need one length per sequence")
+            return [int(x) for x in spec]
+        lo, hi = spec                        # (lo, hi): drawn
+        return torch.randint(int(lo), int(hi) + 1, (B,), generator=g, dtype=torch.int64).tolist()
+
+    lq = draw(lens)
+    lk = lq if lens_k is None else draw(lens_k)
+    total_q, total_k = max(sum(lq), 1), max(sum(lk), 1)
+    q = torch.randn((total_q, Hq, D), generator=g, dtype=torch.float32)
+    k = torch.randn((total_k, Hkv, D), generator=g, dtype=torch.float32)
+    v = torch.randn((total_k, Hkv, D), generator=g, dtype=torch.float32)
+    cq = torch.tensor([0] + lq, dtype=torch.int64).cumsum(0).to(torch.int32)
+    ck = torch.tensor([0] + lk, dtype=torch.int64).cumsum(0).to(torch.int32)
+    return dict(q=_cast(q, dtype), k=_cast(k, dtype), v=_cast(v, dtype), cu_seqlens_q=cq, cu_seqlens_k=ck,
+                max_seqlen_q=max(max(lq), 1), max_seqlen_k=max(max(lk), 1))
+
+
 def make_workload(w, seed=None):
     """Inputs of a named workload (a key of WORKLOADS or a workload object)."""
     if isinstance(w, str):
@@ -122,6 +177,8 @@ def make_workload(w, seed=None):
     s = w.seed if seed is None else seed
     if isinstance(w, DecodeWorkload):
         return make_decode(w.B, w.Hq, w.Hkv, w.D, w.Smax, seed=s, lens=w.lens, dtype=w.dtype)
+    if isinstance(w, VarlenWorkload):
+        return make_varlen(w.B, w.Hq, w.Hkv, w.D, seed=s, lens=w.lens, dtype=w.dtype)
     return make_prefill(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.D, seed=s, lens=w.lens, dtype=w.dtype)
 
 

@@ -53,6 +53,25 @@ def prefill_flops(B, Hq, Sq, Sk, D, causal, seqlens_k=None) -> int:
     return 4 * D * prefill_pairs(B, Hq, Sq, Sk, causal, seqlens_k)
 
 
+def varlen_pairs(Hq: int, lens_q: Sequence[int], lens_k: Sequence[int], causal: bool) -> int:
+    """Admissible (sequence, h, i, j) pairs of packed sequences; causal is
+    bottom-right aligned per sequence (j <= i + Lk - Lq)."""
+    total = 0
+    for lq, lk in zip(lens_q, lens_k):
+        total += prefill_pairs(1, 1, int(lq), int(lk), causal) if lq > 0 and lk > 0 else 0
+    return total * Hq
+
+
+def varlen_flops(Hq, D, lens_q, lens_k, causal) -> int:
+    return 4 * D * varlen_pairs(Hq, lens_q, lens_k, causal)
+
+
+def varlen_bytes(Hq, Hkv, D, total_q, total_k, elem_bytes=2, with_lse=True) -> int:
+    """Q, K, V and out once each (+ fp32 lse)."""
+    b = elem_bytes * D * (2 * total_q * Hq + 2 * total_k * Hkv)
+    return b + (4 * Hq * total_q if with_lse else 0)
+
+
 def prefill_bytes(B, Hq, Hkv, Sq, Sk, D, seqlens_k=None, elem_bytes=2, with_lse=True) -> int:
     """Q read + valid K/V rows read + out written (+ fp32 lse written)."""
     valid_keys = B * Sk if seqlens_k is None else sum(int(x) for x in seqlens_k)

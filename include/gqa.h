@@ -102,6 +102,40 @@ int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
             const int* seqlens_k, int dtype, void* stream);
 
 /*
+ * gqa_fwd_varlen -- gqa_fwd over sequences of different lengths packed
+ * back to back without padding (the BERT batching case: [GQA-BERT]
+ * "阶段二" passes padding_mask / seqlen_k for sequences of unequal length;
+ * packing drops the padded query rows instead of computing and discarding
+ * them).
+ *
+ *   q, out        [total_q, Hq, D]   device; rows cu_seqlens_q[b] ..
+ *                                    cu_seqlens_q[b+1]-1 are sequence b
+ *   k, v          [total_k, Hkv, D]  device; rows cu_seqlens_k[b] ..
+ *   lse           [Hq, total_q] fp32 device, written; may be NULL
+ *   cu_seqlens_q, cu_seqlens_k  int32 [B+1] device, cu[0] = 0, non-
+ *                 decreasing, cu[B] <= total; Lq_b = cu_q[b+1]-cu_q[b] in
+ *                 [0, max_seqlen_q], Lk_b likewise in [0, max_seqlen_k].
+ *                 Values outside these ranges make the affected sequence
+ *                 write nothing and raise GQA_ERR_DEVICE_BOUNDS in
+ *                 gqa_device_status().
+ *   B             number of sequences
+ *   max_seqlen_q, max_seqlen_k  upper bounds of Lq_b / Lk_b (they size the
+ *                 work grid, not the buffers)
+ *   total_q, total_k  rows of the packed tensors (>= 1)
+ *   causal        0, or 1: query i of sequence b sees keys
+ *                 j <= i + Lk_b - Lq_b (bottom-right aligned per sequence)
+ * For sequence b, query head h, query row i (0 <= i < Lq_b) the result is
+ * gqa_fwd's definition with L_b = Lk_b, Sq = Lq_b, Sk = Lk_b; rows of the
+ * packed output that belong to no sequence are not written.
+ * bf16: D 64 or 128, G <= 128, q/k/v/out 16-byte aligned.  fp32: D <= 256.
+ * Concurrency as gqa_fwd.
+ */
+int gqa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float* lse,
+                   const int* cu_seqlens_q, const int* cu_seqlens_k, int B, int Hq, int Hkv,
+                   int max_seqlen_q, int max_seqlen_k, int total_q, int total_k, int D,
+                   float scale, int causal, int dtype, void* stream);
+
+/*
  * gqa_decode_num_splits -- the number of KV-length splits gqa_decode will use.
  * num_splits in 1..128 is returned clamped to the number of 16-key blocks of
  * max_seqlen_k; num_splits <= 0 asks for the automatic choice, which sizes

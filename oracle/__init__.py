@@ -118,3 +118,38 @@ def decode(q, kcache, vcache, cache_seqlens, *, scale=None, rows=None):
     if rows is not None:
         return out, lse
     return out.reshape(B, Hq, D), lse.reshape(B, Hq)
+
+
+def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, scale=None, causal=False):
+    """Oracle GQA attention over sequences packed without padding.
+
+    q [total_q,Hq,D], k/v [total_k,Hkv,D]; cu_seqlens_q/k int [B+1] row offsets.
+    Sequence b is the plain definition of ``attention`` with B = 1, Sq = its
+    query count, Sk = its key count (so causal is bottom-right aligned per
+    sequence), applied to its own rows.  Returns out [total_q,Hq,D] and lse
+    [Hq,total_q] in float64; rows that belong to no sequence stay out = 0,
+    lse = -inf.
+    """
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    total_q, Hq, D = q.shape
+    total_k, Hkv, Dk = k.shape
+    if Dk != D or v.shape != k.shape:
+        raise ValueError("shape mismatch")
+    cq = [int(x) for x in (cu_seqlens_q.tolist() if hasattr(cu_seqlens_q, "tolist") else cu_seqlens_q)]
+    ck = [int(x) for x in (cu_seqlens_k.tolist() if hasattr(cu_seqlens_k, "tolist") else cu_seqlens_k)]
+    if len(cq) != len(ck) or len(cq) < 2:
+        raise ValueError("cu_seqlens must both be [B+1]")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = np.zeros((total_q, Hq, D), np.float64)
+    lse = np.full((Hq, total_q), -np.inf, np.float64)
+    for b in range(len(cq) - 1):
+        q0, q1, k0, k1 = cq[b], cq[b + 1], ck[b], ck[b + 1]
+        if not (0 <= q0 <= q1 <= total_q and 0 <= k0 <= k1 <= total_k):
+            raise ValueError("cu_seqlens out of range at sequence %d" % b)
+        if q1 == q0 or k1 == k0:
+            continue   # no query rows, or no keys: out = 0, lse = -inf
+        o_b, l_b = attention(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1], scale=scale, causal=causal)
+        out[q0:q1] = o_b[0]
+        lse[:, q0:q1] = l_b[0]
+    return out, lse

@@ -53,3 +53,43 @@ def attention(q, k, v, scale, causal=False, seqlens_k=None):
                     out[b][i][h][d] = math.fsum(p * v[b][j][g][d] for p, j in zip(probs, keys))
                 lse[b][h][i] = top + math.log(total)
     return out, lse
+
+
+def attention_packed(q, k, v, cu_q, cu_k, scale, causal=False):
+    """Sequences packed without padding, addressed through their row offsets.
+
+    q[r][h][d] for packed query rows r, k[r][g][d] / v[r][g][d] for packed key
+    rows; sequence b owns query rows cu_q[b] .. cu_q[b+1]-1 and key rows
+    cu_k[b] .. cu_k[b+1]-1.  Query i of sequence b (packed row cu_q[b] + i)
+    attends to its own sequence's keys j (packed row cu_k[b] + j) with, when
+    causal, j <= i + Lk - Lq for that sequence's lengths.  Returns
+    (out[r][h][d], lse[h][r]); rows of no sequence keep out = 0, lse = -inf.
+    """
+    total_q = len(q)
+    Hq = len(q[0])
+    D = len(q[0][0])
+    Hkv = len(k[0])
+    if Hq % Hkv:
+        raise ValueError("Hq must be divisible by Hkv")
+    group = Hq // Hkv
+    out = [[[0.0] * D for _ in range(Hq)] for _ in range(total_q)]
+    lse = [[-math.inf] * total_q for _ in range(Hq)]
+    for b in range(len(cu_q) - 1):
+        q_lo, q_hi = int(cu_q[b]), int(cu_q[b + 1])
+        k_lo, k_hi = int(cu_k[b]), int(cu_k[b + 1])
+        n_q, n_k = q_hi - q_lo, k_hi - k_lo
+        for r in range(q_lo, q_hi):
+            i = r - q_lo
+            for h in range(Hq):
+                g = h // group
+                rows = [k_lo + j for j in range(n_k) if (not causal) or j <= i + n_k - n_q]
+                if not rows:
+                    continue
+                scores = [scale * math.fsum(q[r][h][d] * k[kr][g][d] for d in range(D)) for kr in rows]
+                top = max(scores)
+                weights = [math.exp(s - top) for s in scores]
+                total = math.fsum(weights)
+                for d in range(D):
+                    out[r][h][d] = math.fsum(w / total * v[kr][g][d] for w, kr in zip(weights, rows))
+                lse[h][r] = top + math.log(total)
+    return out, lse

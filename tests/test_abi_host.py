@@ -78,6 +78,27 @@ def test_fwd_fp32_head_dim_limit(lib):
     assert _fwd(lib, D=257, dtype=1) == gqa.GQA_ERR_UNSUPPORTED
 
 
+def _fwd_varlen(lib, B=2, Hq=4, Hkv=2, msq=8, msk=8, tq=12, tk=12, D=64, scale=0.125, causal=0, dtype=0,
+                q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=None, cuq=FAKE, cuk=FAKE):
+    P = ctypes.c_void_p
+    return lib.gqa_fwd_varlen(P(q), P(k), P(v), P(out), P(lse) if lse else None, P(cuq) if cuq else None,
+                              P(cuk) if cuk else None, B, Hq, Hkv, msq, msk, tq, tk, D, scale, causal, dtype,
+                              None)
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(msq=0), dict(msk=0), dict(tq=0), dict(tk=-1), dict(D=0),
+                                dict(Hq=6, Hkv=4), dict(cuq=0), dict(cuk=0), dict(cuq=FAKE + 2),
+                                dict(q=0), dict(out=0), dict(scale=float("nan")), dict(causal=2),
+                                dict(dtype=7), dict(k=FAKE + 8), dict(lse=FAKE + 1)])
+def test_fwd_varlen_rejects_invalid_arguments(lib, kw):
+    assert _fwd_varlen(lib, **kw) == gqa.GQA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(D=96), dict(Hq=129, Hkv=1), dict(D=300, dtype=1)])
+def test_fwd_varlen_unsupported_shapes(lib, kw):
+    assert _fwd_varlen(lib, **kw) == gqa.GQA_ERR_UNSUPPORTED
+
+
 def _dec(lib, B=2, Hq=8, Hkv=2, D=128, scale=0.1, ns=1, smax=64, dtype=0, ws=None, wsb=0, q=FAKE,
          lens=FAKE):
     P = ctypes.c_void_p

@@ -349,3 +349,76 @@ def test_flop_model_counts_only_admissible_pairs():
     assert roofline.prefill_pairs(1, 1, 7, 7, True) == 28
     assert roofline.prefill_pairs(2, 3, 5, 5, False, [5, 2]) == 3 * 5 * 7
     assert roofline.prefill_flops(4, 32, 8192, 8192, 128, True) == 4 * 4 * 32 * 128 * 8192 * 8193 // 2
+
+
+# ------------------------------------------------------ packed (varlen) oracle
+
+def _varlen_cases(n, seed):
+    rng = random.Random(seed)
+    cases = []
+    for _ in range(n):
+        Hkv = rng.choice([1, 2])
+        G = rng.choice([1, 2, 3, 4])
+        B = rng.randint(1, 4)
+        lq = [rng.choice([0, 1, 2, 5, 9]) for _ in range(B)]
+        lk = [rng.choice([0, 1, 3, 6, 11]) for _ in range(B)]
+        spare = rng.choice([0, 0, 2])      # packed rows after the last sequence
+        if sum(lq) + spare == 0:
+            spare = 1                       # at least one packed query row
+        cases.append((B, G * Hkv, Hkv, lq, lk, spare, rng.choice([1, 4, 8]), rng.random() < 0.5,
+                      rng.choice([0.35, -0.6, 1.3]), rng.randint(0, 1 << 30)))
+    return cases
+
+
+def _cu(lens):
+    return [0] + list(np.cumsum(lens).astype(int))
+
+
+@pytest.mark.parametrize("case", _varlen_cases(60, 777))
+def test_varlen_oracle_matches_packed_brute_force(case):
+    B, Hq, Hkv, lq, lk, spare, D, causal, scale, seed = case
+    rng = np.random.default_rng(seed)
+    tq, tk = sum(lq) + spare, max(sum(lk), 1)
+    q, k, v = _rand((tq, Hq, D), rng), _rand((tk, Hkv, D), rng), _rand((tk, Hkv, D), rng)
+    cq, ck = _cu(lq), _cu(lk)
+    out, lse = oracle.attention_varlen(q, k, v, cq, ck, scale=scale, causal=causal)
+    bo, bl = brute.attention_packed(_tolist(q), _tolist(k), _tolist(v), cq, ck, scale, causal)
+    np.testing.assert_allclose(out, np.array(bo), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, np.array(bl), rtol=1e-12, atol=1e-12)
+
+
+def test_varlen_equals_padded_dense_oracle_exactly():
+    # every sequence has Sq query rows; keys are right-padded to Sk in the
+    # dense batch and given per sequence through seqlens_k
+    rng = np.random.default_rng(5)
+    B, Hq, Hkv, Sq, Sk, D = 3, 8, 2, 7, 13, 16
+    lk = [13, 4, 9]
+    qd = _rand((B, Sq, Hq, D), rng)
+    kd, vd = _rand((B, Sk, Hkv, D), rng), _rand((B, Sk, Hkv, D), rng)
+    od, ld = oracle.attention(qd, kd, vd, scale=0.2, seqlens_k=np.array(lk, np.int32))
+    qp = qd.reshape(B * Sq, Hq, D)
+    kp = np.concatenate([kd[b, :lk[b]] for b in range(B)])
+    vp = np.concatenate([vd[b, :lk[b]] for b in range(B)])
+    op, lp = oracle.attention_varlen(qp, kp, vp, _cu([Sq] * B), _cu(lk), scale=0.2)
+    assert np.array_equal(op.reshape(B, Sq, Hq, D), od)
+    assert np.array_equal(lp.reshape(Hq, B, Sq).transpose(1, 0, 2), ld)
+
+
+def test_varlen_sequence_order_permutes_rows_exactly():
+    rng = np.random.default_rng(9)
+    lq, lk, Hq, Hkv, D = [3, 5, 2], [4, 2, 6], 4, 2, 8
+    seqs = [(_rand((lq[b], Hq, D), rng), _rand((lk[b], Hkv, D), rng), _rand((lk[b], Hkv, D), rng))
+            for b in range(3)]
+
+    def run(order):
+        q = np.concatenate([seqs[b][0] for b in order])
+        k = np.concatenate([seqs[b][1] for b in order])
+        v = np.concatenate([seqs[b][2] for b in order])
+        o, l = oracle.attention_varlen(q, k, v, _cu([lq[b] for b in order]), _cu([lk[b] for b in order]),
+                                       scale=0.4, causal=True)
+        starts = dict(zip(order, _cu([lq[b] for b in order])))
+        return {b: (o[starts[b]:starts[b] + lq[b]], l[:, starts[b]:starts[b] + lq[b]]) for b in order}
+
+    a, b_ = run([0, 1, 2]), run([2, 0, 1])
+    for s in range(3):
+        assert np.array_equal(a[s][0], b_[s][0]) and np.array_equal(a[s][1], b_[s][1])
