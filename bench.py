@@ -290,6 +290,40 @@ def time_prefill_workload(gqa, name, device, flush, reps=10, warmup=3):
             "algorithmic_flops_per_launch": flops}
 
 
+def time_decode_fp8(gqa, name, device, flush, reps=20, warmup=3):
+    """Per-call time of gqa_decode_fp8 (split + combine) on a named FP8-cache
+    decode workload, L2 flushed before every call; returns GB/s of e4m3 KV bytes."""
+    w = inputs.WORKLOADS[name]
+    inp = inputs.make_workload(w)
+    d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    lens = inp["cache_seqlens"].tolist()
+    kv_bytes = roofline.decode_kv_bytes(w.Hkv, w.D, lens, elem_bytes=1)
+    out = torch.empty_like(d["q"])
+    wsb = gqa.gqa_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, 0, w.Smax)
+    work = torch.empty((max(wsb, 16),), dtype=torch.uint8, device=device)
+
+    def call():
+        gqa.gqa_decode_fp8(d["q"], d["kcache"], d["vcache"], d["cache_seqlens"], d["k_scale"], d["v_scale"],
+                           scale=w.scale, out=out, workspace=work)
+
+    for _ in range(warmup):
+        flush.fill_(1)
+        call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record()
+        call()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / reps
+    return {"value": kv_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s (e4m3 KV-cache bytes read / decode time)",
+            "ms": ms, "kv_bytes_per_step": kv_bytes,
+            "tokens_per_s": sum(lens) / (ms * 1e-3),
+            "workload": "%s decode B%d Hq%d Hkv%d D%d Smax%d cache lengths U[%d,%d], FP8 e4m3 cache" % (
+                w.name, w.B, w.Hq, w.Hkv, w.D, w.Smax, w.lens[0], w.lens[1])}
+
+
 def _workload_name(w):
     if isinstance(w, inputs.VarlenWorkload):
         return "%s packed prefill B%d Hq%d Hkv%d D%d %s lengths U[%d,%d] (queries = keys), no padding" % (
@@ -452,6 +486,7 @@ def main():
 
     # ---- the other prefill workloads, timed the same way (not part of `value`)
     others = {}
+    dec8 = None
     if not args.no_other_workloads:
         del P, pin, out_p, lse_p
         for name in ("bert_base", "bert_large_long", "causal_long", "bert_base_varlen"):
@@ -459,6 +494,7 @@ def main():
                 others[name] = {"tflops": value / ws, "ms": pre_avg * 1e3}
                 continue
             others[name] = time_prefill_workload(gqa, name, device, flush, reps=args.other_reps)
+        dec8 = time_decode_fp8(gqa, "llama_decode_fp8", device, flush)
         torch.cuda.synchronize()
         if gqa.gqa_device_status() != 0:
             raise RuntimeError("device error while timing the other prefill workloads")
@@ -487,6 +523,7 @@ def main():
             "gpu_launches": launches_per_step * K,
             "cpu_baseline": cb,
             "prefill_workloads": others,
+            "decode_fp8": dec8,
         }
         print(json.dumps(line))
     if ws > 1:

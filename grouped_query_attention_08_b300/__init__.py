@@ -63,6 +63,9 @@ def load_library():
         lib.gqa_fwd_varlen.restype = i32
         lib.gqa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
                                        f32, i32, i32, vp]
+        lib.gqa_decode_fp8.restype = i32
+        lib.gqa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, i32, vp, sz,
+                                       vp]
         lib.gqa_decode.restype = i32
         lib.gqa_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, vp, sz, vp]
         lib.gqa_decode_num_splits.restype = i32
@@ -248,6 +251,44 @@ def gqa_decode(q, kcache, vcache, cache_seqlens, *, scale=None, num_splits=0, ou
                                    _ptr(workspace), wbytes, _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_decode")
+    return out
+
+
+def gqa_decode_fp8(q, kcache, vcache, cache_seqlens, k_scale, v_scale, *, scale=None, num_splits=0, out=None,
+                   workspace=None, stream=None):
+    """Single-token decode over an FP8 (e4m3) cache.  q [B,Hq,128] bf16; caches
+    [B,Smax,Hkv,128] torch.float8_e4m3fn (or uint8 holding e4m3 bytes); the cached
+    key is k_scale * kcache and the value v_scale * vcache.  Returns out [B,Hq,128] bf16.
+    """
+    torch = _torch()
+    if q.dim() != 3 or kcache.dim() != 4 or vcache.dim() != 4:
+        raise ValueError("q must be [B,Hq,D] and caches [B,Smax,Hkv,D]")
+    B, Hq, D = q.shape
+    Bk, Smax, Hkv, Dk = kcache.shape
+    if Bk != B or Dk != D or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("shape mismatch between q and the caches")
+    if q.dtype != torch.bfloat16:
+        raise TypeError("q must be bfloat16")
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    for c in (kcache, vcache):
+        if c.dtype not in (torch.uint8, f8):
+            raise TypeError("the caches must be float8_e4m3fn (or uint8 e4m3 bytes)")
+    if cache_seqlens.dtype != torch.int32 or tuple(cache_seqlens.shape) != (B,):
+        raise ValueError("cache_seqlens must be int32 [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    need = gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, Smax)
+    if workspace is None and need > 0:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
+    dev = _check_cuda(q, kcache, vcache, cache_seqlens, out, workspace)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = load_library().gqa_decode_fp8(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_seqlens), _ptr(out),
+                                       B, Hq, Hkv, D, float(scale), float(k_scale), float(v_scale),
+                                       int(num_splits), Smax, _ptr(workspace), wbytes, _stream(dev, stream))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_decode_fp8")
     return out
 
 

@@ -1,0 +1,327 @@
+// decode_fp8_sm103.cuh -- single-token GQA decode over an FP8 (e4m3) KV
+// cache: the same split-KV method as decode_sm103.cuh with half the cache
+// bytes.
+//
+// Sources (page title and section):
+//  * GQA paper summary (azimuth.plus/paper/gqa), "Problem" / "Bottleneck":
+//    a generation step reads the whole KV cache and is bound by memory
+//    bandwidth; a smaller cache entry is a proportionally faster step.
+//  * "3个GQA核心优化技巧" (blog.gitcode.com): quantisation named as a way to
+//    compress the cache further; "阶段二" for split-KV (num_splits).
+//  * "FlashAttention Serisi" (webturing.pages.dev), "Ana fikir": running
+//    max / sum per split, partials merged through their log-sum-exp.
+//
+// Cache values are e4m3 with one scale per tensor: the attended key is
+// k_scale * k8 and the value v_scale * v8.  Hence
+//   s = scale * q.(k_scale k8) = (scale * k_scale) * q.k8
+//   out = sum p v_scale v8 / l = v_scale * (sum p v8 / l)
+// so k_scale folds into the softmax scale and v_scale into the output.
+//
+// Matrix products run on mma.sync m16n8k16 in f16: every e4m3 value is
+// exact in f16 (cvt.rn.f16x2.e4m3x2), q is brought into f16's range by an
+// exact power-of-two scaling 2^e of the whole group (2^-e folds into the
+// score scale), and P in [0, 1] is held in f16.  Accumulation is fp32.
+// Head dimension 128: a lane then reads exactly one 16-byte chunk of each
+// of its four V rows per 16-key block.
+#pragma once
+
+#include "decode_sm103.cuh"
+
+namespace gqa {
+namespace decode {
+
+constexpr int kF8D = 128;
+
+struct ParamsF8 {
+  const __nv_bfloat16* q;       // [B, Hq, 128]
+  const uint8_t* kc;            // [B, Smax, Hkv, 128] e4m3
+  const uint8_t* vc;            // [B, Smax, Hkv, 128] e4m3
+  const int* seqlens;           // [B]
+  __nv_bfloat16* out;           // [B, Hq, 128]         (nsplit == 1)
+  float* part_o;                // [B, Hq, nsplit, 128] (nsplit > 1)
+  float* part_lse;              // [B, Hq, nsplit]
+  int B, Hq, Hkv, G, Smax;
+  int nsplit, split_len;
+  float scale_k_log2;           // scale * k_scale * log2(e)
+  float v_scale;
+};
+
+// Per-warp ring of 16-key blocks, K rows then V rows, 128 bytes per row,
+// chunks XOR-swizzled with swz() as in the bf16 ring.
+struct RingF8 {
+  static constexpr int kRing = 6;                          // 5 blocks in flight per warp
+  static constexpr uint32_t kRowBytes = kF8D;
+  static constexpr uint32_t kSlotBytes = 2 * kBlockKeys * kRowBytes;
+  static constexpr uint32_t kWarpBytes = kRing * kSlotBytes;
+  static constexpr uint32_t kBytes = kWarps * kWarpBytes;
+};
+
+// two e4m3 values (low byte, high byte) -> f16x2 (low half, high half)
+DEVI void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+      "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(w));
+}
+
+DEVI uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+DEVI void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                        uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Asynchronous copy of the 16-key block at key k0 into a ring slot; keys >=
+// kend are zero-filled (source clamped to the valid row kvalid, 0 bytes read).
+DEVI void issue_block_f8(uint32_t slot, const uint8_t* kbase, const uint8_t* vbase, size_t row_stride, int k0,
+                         int kend, int kvalid, int lane) {
+  constexpr int kChunks = kF8D / 16;
+  constexpr int kPerLane = 2 * kBlockKeys * kChunks / 32;
+#pragma unroll
+  for (int i = 0; i < kPerLane; ++i) {
+    const int id = lane + 32 * i;
+    const int row = id / kChunks, chunk = id % kChunks;   // rows 0-15 K, 16-31 V
+    const int key = k0 + (row & (kBlockKeys - 1));
+    const bool ok = key < kend;
+    const uint8_t* src = (row < kBlockKeys ? kbase : vbase) + size_t(ok ? key : kvalid) * row_stride + 16 * chunk;
+    cp_async_16(slot + uint32_t(row) * RingF8::kRowBytes + (uint32_t(chunk) ^ swz(row)) * 16u, src, ok ? 16u : 0u);
+  }
+  cp_async_commit();
+}
+
+// Raw e4m3 fragments of a block: K rows (r, r+8) chunks (c, c+4); V rows
+// (2c, 2c+1, 2c+8, 2c+9) chunk r.
+struct BlockF8 {
+  uint4 k[2][2];
+  uint4 v[4];
+};
+
+DEVI void fetch_block_f8(BlockF8& R, uint32_t slot, int r, int c) {
+  constexpr uint32_t RB = RingF8::kRowBytes;
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int row = r + 8 * h;
+      R.k[h][q] = lds128(slot + uint32_t(row) * RB + (uint32_t(c + 4 * q) ^ swz(row)) * 16u);
+    }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int row = kBlockKeys + 2 * c + (i & 1) + 8 * (i >> 1);
+    R.v[i] = lds128(slot + uint32_t(row) * RB + (uint32_t(r) ^ swz(row)) * 16u);
+  }
+}
+
+__global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const ParamsF8 p) {
+  constexpr int D = kF8D;
+  constexpr int KS = D / 16;      // k-steps of QK^T
+  constexpr int MT = D / 16;      // m-tiles of O^T
+  const int split = blockIdx.x;
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int r = lane >> 2;
+  const int c = lane & 3;
+
+  int Lb = p.seqlens[b];
+  if (Lb < 0 || Lb > p.Smax) {
+    if (split == 0 && kvh == 0 && threadIdx.x == 0) raise_error(kErrBounds);
+    Lb = 0;
+  }
+  const int kstart = split * p.split_len;
+  if (kstart >= Lb && p.nsplit > 1) return;  // empty split: the combine skips it
+  const int kend = min(Lb, kstart + p.split_len);
+  const int nblk = kend > kstart ? (kend - kstart + kBlockKeys - 1) / kBlockKeys : 0;
+
+  // Q^T fragments (head n = r; zero if n >= G), dims d0..d0+3 of k-step ks
+  // with d0 = 16 (c + 4 (ks / 4)) + 4 (ks % 4) -- the order in which the K
+  // chunks below deliver them.  The whole group is scaled by 2^e so that its
+  // largest |q| lies below 2^15 (exact; 2^-e goes into the score scale).
+  float qv[KS][4];
+  float qmax = 0.f;
+  {
+    const bool hv = r < p.G;
+    const __nv_bfloat16* qrow = p.q + (size_t(b) * p.Hq + size_t(kvh) * p.G + (hv ? r : 0)) * D;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const int d0 = 16 * (c + 4 * (ks >> 2)) + 4 * (ks & 3);
+      const uint2 w = hv ? *reinterpret_cast<const uint2*>(qrow + d0) : make_uint2(0u, 0u);
+      qv[ks][0] = __uint_as_float(w.x << 16);
+      qv[ks][1] = __uint_as_float(w.x & 0xffff0000u);
+      qv[ks][2] = __uint_as_float(w.y << 16);
+      qv[ks][3] = __uint_as_float(w.y & 0xffff0000u);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) qmax = fmaxf(qmax, fabsf(qv[ks][e]));
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, off));
+  int ex = 0;
+  if (qmax > 0.f && qmax < INFINITY) {
+    frexpf(qmax, &ex);                     // qmax < 2^ex
+    ex = max(-120, min(120, 15 - ex));     // 2^ex * qmax < 2^15
+  }
+  const float up = ldexpf(1.f, ex);
+  uint32_t qf[KS][2];
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    qf[ks][0] = pack_f16x2(qv[ks][0] * up, qv[ks][1] * up);
+    qf[ks][1] = pack_f16x2(qv[ks][2] * up, qv[ks][3] * up);
+  }
+  const float cl = p.scale_k_log2 * ldexpf(1.f, -ex);
+
+  const size_t row_stride = size_t(p.Hkv) * D;                       // bytes
+  const uint8_t* kbase = p.kc + (size_t(b) * p.Smax * p.Hkv + kvh) * D;
+  const uint8_t* vbase = p.vc + (size_t(b) * p.Smax * p.Hkv + kvh) * D;
+
+  float o[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;   // heads 2c and 2c+1
+
+  using RG = RingF8;
+  extern __shared__ __align__(16) uint8_t dsmem[];
+  const uint32_t ring = smem_u32(dsmem) + uint32_t(warp) * RG::kWarpBytes;
+#pragma unroll
+  for (int i = 0; i < RG::kRing - 1; ++i) {
+    const int bi = warp + i * kWarps;
+    if (bi < nblk)
+      issue_block_f8(ring + uint32_t(i) * RG::kSlotBytes, kbase, vbase, row_stride, kstart + bi * kBlockKeys, kend,
+                     kstart, lane);
+    else
+      cp_async_commit();
+  }
+  BlockF8 cur;
+  int it = 0;
+  for (int blk = warp; blk < nblk; blk += kWarps, ++it) {
+    cp_async_wait<RG::kRing - 2>();
+    __syncwarp();
+    fetch_block_f8(cur, ring + uint32_t(it % RG::kRing) * RG::kSlotBytes, r, c);
+    __syncwarp();
+    {
+      const int nb = blk + (RG::kRing - 1) * kWarps;
+      const uint32_t slot = ring + uint32_t((it + RG::kRing - 1) % RG::kRing) * RG::kSlotBytes;
+      if (nb < nblk)
+        issue_block_f8(slot, kbase, vbase, row_stride, kstart + nb * kBlockKeys, kend, kstart, lane);
+      else
+        cp_async_commit();
+    }
+    const int k0 = kstart + blk * kBlockKeys;
+
+    // S^T = K . Q^T: k-step ks = 4 q + j uses raw word j of chunk c + 4q
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t a0, a2, a1, a3;
+        e4m3x4_to_f16x2x2(word(cur.k[0][q], j), a0, a2);
+        e4m3x4_to_f16x2x2(word(cur.k[1][q], j), a1, a3);
+        mma_f16_16816(s, a0, a1, a2, a3, qf[4 * q + j][0], qf[4 * q + j][1]);
+      }
+    const bool v0 = (k0 + r) < kend, v1 = (k0 + r + 8) < kend;
+    const float tA0 = v0 ? s[0] * cl : -INFINITY, tB0 = v0 ? s[1] * cl : -INFINITY;
+    const float tA1 = v1 ? s[2] * cl : -INFINITY, tB1 = v1 ? s[3] * cl : -INFINITY;
+    float xA = fmaxf(tA0, tA1), xB = fmaxf(tB0, tB1);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, off));
+      xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, off));
+    }
+    const float nA = fmaxf(mA, xA), nB = fmaxf(mB, xB);
+    const float rA = (nA == -INFINITY) ? 0.f : nA, rB = (nB == -INFINITY) ? 0.f : nB;
+    const float aA = ex2_approx(mA - rA), aB = ex2_approx(mB - rB);
+    mA = nA;
+    mB = nB;
+    const float pA0 = ex2_approx(tA0 - rA), pA1 = ex2_approx(tA1 - rA);
+    const float pB0 = ex2_approx(tB0 - rB), pB1 = ex2_approx(tB1 - rB);
+    lA = lA * aA + pA0 + pA1;
+    lB = lB * aB + pB0 + pB1;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      o[mt][0] *= aA;
+      o[mt][1] *= aB;
+      o[mt][2] *= aA;
+      o[mt][3] *= aB;
+    }
+    const uint32_t pb0 = movmatrix_trans(pack_f16x2(pA0, pB0));
+    const uint32_t pb1 = movmatrix_trans(pack_f16x2(pA1, pB1));
+    // O^T += V^T . P^T: m-tile mt rows r / r+8 are dims 16 r + 2 mt (+1),
+    // taken from f16 word mt of each V row's chunk
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      uint32_t lo[4], hi[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) e4m3x4_to_f16x2x2(word(cur.v[i], wi), lo[i], hi[i]);
+      mma_f16_16816(o[2 * wi], __byte_perm(lo[0], lo[1], 0x5410), __byte_perm(lo[0], lo[1], 0x7632),
+                    __byte_perm(lo[2], lo[3], 0x5410), __byte_perm(lo[2], lo[3], 0x7632), pb0, pb1);
+      mma_f16_16816(o[2 * wi + 1], __byte_perm(hi[0], hi[1], 0x5410), __byte_perm(hi[0], hi[1], 0x7632),
+                    __byte_perm(hi[2], hi[3], 0x5410), __byte_perm(hi[2], hi[3], 0x7632), pb0, pb1);
+    }
+  }
+  cp_async_wait<0>();
+
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    lA += __shfl_xor_sync(0xffffffffu, lA, off);
+    lB += __shfl_xor_sync(0xffffffffu, lB, off);
+  }
+
+  // ---- merge the 4 warps through shared memory (the rings are done)
+  __syncthreads();
+  float (*s_o)[8][D] = reinterpret_cast<float (*)[8][D]>(dsmem);
+  float (*s_m)[8] = reinterpret_cast<float (*)[8]>(dsmem + sizeof(float) * kWarps * 8 * D);
+  float (*s_l)[8] = reinterpret_cast<float (*)[8]>(dsmem + sizeof(float) * (kWarps * 8 * D + kWarps * 8));
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) {
+    const int d_lo = 16 * r + 2 * mt;
+    s_o[warp][2 * c][d_lo] = o[mt][0];
+    s_o[warp][2 * c + 1][d_lo] = o[mt][1];
+    s_o[warp][2 * c][d_lo + 1] = o[mt][2];
+    s_o[warp][2 * c + 1][d_lo + 1] = o[mt][3];
+  }
+  if (r == 0) {
+    s_m[warp][2 * c] = mA;
+    s_m[warp][2 * c + 1] = mB;
+    s_l[warp][2 * c] = lA;
+    s_l[warp][2 * c + 1] = lB;
+  }
+  __syncthreads();
+
+  const int G = p.G;
+  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
+    const int n = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][n]);
+    const float Mr = (M == -INFINITY) ? 0.f : M;
+    float num = 0.f, den = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float f = ex2_approx(s_m[w][n] - Mr);
+      num += f * s_o[w][n][d];
+      den += f * s_l[w][n];
+    }
+    const float val = den > 0.f ? num / den * p.v_scale : 0.f;
+    const size_t hrow = size_t(b) * p.Hq + size_t(kvh) * G + n;
+    if (p.nsplit == 1) {
+      p.out[hrow * D + d] = __float2bfloat16_rn(val);
+    } else {
+      p.part_o[(hrow * p.nsplit + split) * D + d] = val;
+      if (d == 0)
+        p.part_lse[hrow * p.nsplit + split] = den > 0.f ? (Mr + log2f(den)) * 0.6931471805599453f : -INFINITY;
+    }
+  }
+}
+
+}  // namespace decode
+}  // namespace gqa

@@ -16,6 +16,7 @@
 #include "common.cuh"
 #include "prefill_sm103.cuh"
 #include "decode_sm103.cuh"
+#include "decode_fp8_sm103.cuh"
 #include "fp32_check.cuh"
 
 namespace {
@@ -214,6 +215,18 @@ bool decode_smem_attr_set(int dev) {
   return true;
 }
 
+bool decode_fp8_smem_attr_set(int dev) {
+  static bool done[kMaxDevices] = {false};
+  if (dev >= 0 && dev < kMaxDevices && done[dev]) return true;
+  if (cudaFuncSetAttribute(gqa::decode::decode_split_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(gqa::decode::RingF8::kBytes)) != cudaSuccess)
+    return false;
+  if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
+  return true;
+}
+static_assert(gqa::decode::RingF8::kBytes >= sizeof(float) * (gqa::decode::kWarps * 8 * 128 + 2 * gqa::decode::kWarps * 8),
+              "the fp8 decode merge reuses the ring memory");
+
 int launch_f32(const gqa::f32::Params& p, cudaStream_t stream) {
   const long long rows = p.cu_q ? (long long)p.Hq * p.total_q : (long long)p.B * p.Hq * p.Sq;
   const long long gx = (rows + gqa::f32::kWarps - 1) / gqa::f32::kWarps;
@@ -380,6 +393,56 @@ int gqa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float
     return launch_f32(p, st);
   }
   return GQA_ERR_INVALID_ARG;
+}
+
+int gqa_decode_fp8(const void* q, const void* kcache, const void* vcache, const int* cache_seqlens, void* out,
+                   int B, int Hq, int Hkv, int D, float scale, float k_scale, float v_scale, int num_splits,
+                   int max_seqlen_k, void* workspace, size_t workspace_bytes, void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_seqlen_k <= 0) return GQA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0 || num_splits > kMaxSplits) return GQA_ERR_INVALID_ARG;
+  if (!q || !kcache || !vcache || !cache_seqlens || !out) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !std::isfinite(k_scale) || !std::isfinite(v_scale) || !aligned(cache_seqlens, 4))
+    return GQA_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(kcache, 16) || !aligned(vcache, 16) || !aligned(out, 16)) return GQA_ERR_INVALID_ARG;
+  const int G = Hq / Hkv;
+  if (D != gqa::decode::kF8D || G > 8) return GQA_ERR_UNSUPPORTED;
+  if (B > 65535 || Hkv > 65535) return GQA_ERR_UNSUPPORTED;
+  const SplitPlan sp = plan_splits(B, Hkv, max_seqlen_k, num_splits);
+  const size_t need = workspace_for(B, Hq, D, sp.n);
+  if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16))) return GQA_ERR_INVALID_ARG;
+  float* part_o = static_cast<float*>(workspace);
+  float* part_lse = need ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                                    ((size_t(B) * Hq * sp.n * D * sizeof(float) + 255) / 256) * 256)
+                         : nullptr;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  gqa::decode::ParamsF8 p;
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.kc = static_cast<const uint8_t*>(kcache);
+  p.vc = static_cast<const uint8_t*>(vcache);
+  p.seqlens = cache_seqlens;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.part_o = part_o;
+  p.part_lse = part_lse;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = G;
+  p.Smax = max_seqlen_k;
+  p.nsplit = sp.n;
+  p.split_len = sp.len;
+  p.scale_k_log2 = float(double(scale) * double(k_scale) * 1.4426950408889634);
+  p.v_scale = v_scale;
+  if (!decode_fp8_smem_attr_set(current_device())) return GQA_ERR_CUDA;
+  gqa::decode::decode_split_fp8_kernel<<<dim3(sp.n, Hkv, B), gqa::decode::kThreads, gqa::decode::RingF8::kBytes,
+                                         st>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  if (sp.n > 1) {
+    const int rows = B * Hq;
+    gqa::decode::combine_kernel<__nv_bfloat16, 4><<<(rows + 3) / 4, 128, 0, st>>>(
+        part_o, part_lse, cache_seqlens, static_cast<__nv_bfloat16*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
+    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  }
+  return GQA_OK;
 }
 
 int gqa_decode_num_splits(int B, int Hkv, int max_seqlen_k, int num_splits) {

@@ -93,6 +93,10 @@ WORKLOADS = {
     "llama_decode_small": DecodeWorkload("llama_decode_small", 16, 64, 8, 128, 8192, (1024, 8192), "bf16", 3),
     # long causal prefill, D=128
     "causal_long": PrefillWorkload("causal_long", 4, 32, 8, 8192, 8192, 128, True, None, "bf16", 4),
+    # llama_decode with the cache quantised to FP8 e4m3 (one scale per tensor)
+    "llama_decode_fp8": DecodeWorkload("llama_decode_fp8", 64, 64, 8, 128, 8192, (1024, 8192), "fp8kv", 3),
+    "llama_decode_fp8_small": DecodeWorkload("llama_decode_fp8_small", 16, 64, 8, 128, 8192, (1024, 8192),
+                                             "fp8kv", 3),
     # bert_base's batch packed without padding: each sequence's query and key
     # length ~ U[512,1024]
     "bert_base_varlen": VarlenWorkload("bert_base_varlen", 32, 12, 3, 64, False, (512, 1024), "bf16", 1),
@@ -170,11 +174,34 @@ def make_varlen(B, Hq, Hkv, D, *, seed=0, lens=(1, 16), lens_k=None, dtype="bf16
                 max_seqlen_q=max(max(lq), 1), max_seqlen_k=max(max(lk), 1))
 
 
+def quantize_e4m3(x: torch.Tensor):
+    """Per-tensor FP8 e4m3 quantisation as a caller would do it: scale =
+    max|x| / 448 (rounded to float32), values round(x / scale) to e4m3 by
+    round-to-nearest-even, clamped to the finite range.  Returns (x8, scale)."""
+    amax = float(x.abs().max())
+    scale = float(torch.tensor(amax / 448.0 if amax > 0 else 1.0, dtype=torch.float32))
+    x8 = (x / scale).clamp(-448.0, 448.0).to(torch.float8_e4m3fn)
+    return x8, scale
+
+
+def make_decode_fp8(B, Hq, Hkv, D, Smax, *, seed=0, lens=(1, None), q_mult=1.0):
+    """make_decode's draws with the caches quantised to e4m3: dict(q bf16 [B,Hq,D],
+    kcache, vcache float8_e4m3fn [B,Smax,Hkv,D], k_scale, v_scale, cache_seqlens)."""
+    d = make_decode(B, Hq, Hkv, D, Smax, seed=seed, lens=lens, dtype="fp32")
+    k8, ks = quantize_e4m3(d["kcache"])
+    v8, vs = quantize_e4m3(d["vcache"])
+    q = d["q"] * float(q_mult) if q_mult != 1.0 else d["q"]
+    return dict(q=q.to(torch.bfloat16), kcache=k8, vcache=v8, k_scale=ks, v_scale=vs,
+                cache_seqlens=d["cache_seqlens"])
+
+
 def make_workload(w, seed=None):
     """Inputs of a named workload (a key of WORKLOADS or a workload object)."""
     if isinstance(w, str):
         w = WORKLOADS[w]
     s = w.seed if seed is None else seed
+    if isinstance(w, DecodeWorkload) and w.dtype == "fp8kv":
+        return make_decode_fp8(w.B, w.Hq, w.Hkv, w.D, w.Smax, seed=s, lens=w.lens)
     if isinstance(w, DecodeWorkload):
         return make_decode(w.B, w.Hq, w.Hkv, w.D, w.Smax, seed=s, lens=w.lens, dtype=w.dtype)
     if isinstance(w, VarlenWorkload):

@@ -189,6 +189,30 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache,
                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gqa_decode_fp8 -- gqa_decode over a KV cache stored as FP8 e4m3 (one byte
+ * per value), half the bytes of a bf16 cache.  [GQA-PAPER] "Problem" /
+ * "Bottleneck" (the step reads the whole cache, so its size sets the time);
+ * [GQA-BERT] names quantisation of the cache as further compression.
+ *
+ *   q              [B, Hq, 128] bf16   device, read
+ *   kcache, vcache [B, Smax, Hkv, 128] e4m3 (OCP FP8 E4M3, finite values
+ *                  only, max 448) device, read
+ *   k_scale, v_scale  one scale per tensor: the cached key is
+ *                  k_scale * kcache and the value v_scale * vcache (the
+ *                  caller quantises x as round(x / scale) to e4m3)
+ *   everything else as gqa_decode (bf16 out, cache_seqlens, scale,
+ *   num_splits, max_seqlen_k, workspace of gqa_decode_workspace_bytes(B,
+ *   Hq, Hkv, 128, num_splits, max_seqlen_k) bytes).
+ * Result: gqa_decode's definition on the dequantised cache.  D must be 128
+ * and G <= 8 (GQA_ERR_UNSUPPORTED otherwise); q/out/caches 16-byte aligned;
+ * scale, k_scale and v_scale finite (GQA_ERR_INVALID_ARG otherwise).
+ */
+int gqa_decode_fp8(const void* q, const void* kcache, const void* vcache,
+                   const int* cache_seqlens, void* out, int B, int Hq, int Hkv, int D,
+                   float scale, float k_scale, float v_scale, int num_splits, int max_seqlen_k,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * gqa_decode_noalloc -- gqa_decode for callers that cannot allocate device
  * memory.  The pages have no counterpart to this entry point.
  *

@@ -153,3 +153,23 @@ def attention_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, scale=None, causal=
         out[q0:q1] = o_b[0]
         lse[:, q0:q1] = l_b[0]
     return out, lse
+
+
+def decode_fp8(q, kcache8, vcache8, k_scale, v_scale, cache_seqlens, *, scale=None, rows=None):
+    """Oracle decode over an e4m3 cache with one scale per tensor: the attended
+    key is k_scale * k8 and the value v_scale * v8.
+
+    Since scale * q.(k_scale k8) = (scale * k_scale) * q.k8 and the output is
+    linear in V, this is ``decode`` on the e4m3 values themselves (exact in
+    float32) with the softmax scale scale * k_scale (in fp64), its output
+    multiplied by v_scale (in fp64); lse is unchanged.
+    """
+    def f8(a):
+        if hasattr(a, "detach"):
+            return a.detach().cpu().float().numpy()
+        return np.asarray(a, dtype=np.float32)
+    q = _f32(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(q.shape[-1])
+    out, lse = decode(q, f8(kcache8), f8(vcache8), cache_seqlens, scale=float(scale) * float(k_scale), rows=rows)
+    return out * float(v_scale), lse

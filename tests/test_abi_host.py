@@ -133,3 +133,22 @@ def test_split_planning(lib):
     assert gqa.gqa_decode_workspace_bytes(64, 64, 8, 128, 1, 8192) == 0
     ws = gqa.gqa_decode_workspace_bytes(64, 64, 8, 128, 8, 8192)
     assert ws >= 64 * 64 * 8 * 129 * 4
+
+
+def _dec8(lib, B=2, Hq=8, Hkv=2, D=128, scale=0.1, ks=0.01, vs=0.02, ns=1, smax=64, ws=None, wsb=0, q=FAKE,
+          kc=FAKE, lens=FAKE):
+    P = ctypes.c_void_p
+    return lib.gqa_decode_fp8(P(q), P(kc), P(FAKE), P(lens) if lens else None, P(FAKE), B, Hq, Hkv, D, scale,
+                              ks, vs, ns, smax, P(ws) if ws else None, wsb, None)
+
+
+def test_decode_fp8_validation(lib):
+    assert _dec8(lib, Hq=6, Hkv=4) == gqa.GQA_ERR_INVALID_ARG
+    assert _dec8(lib, lens=0) == gqa.GQA_ERR_INVALID_ARG
+    assert _dec8(lib, kc=FAKE + 8) == gqa.GQA_ERR_INVALID_ARG          # caches 16-byte aligned
+    assert _dec8(lib, ks=float("inf")) == gqa.GQA_ERR_INVALID_ARG
+    assert _dec8(lib, vs=float("nan")) == gqa.GQA_ERR_INVALID_ARG
+    assert _dec8(lib, ns=129) == gqa.GQA_ERR_INVALID_ARG
+    assert _dec8(lib, D=64) == gqa.GQA_ERR_UNSUPPORTED                 # head dimension 128 only
+    assert _dec8(lib, Hq=32, Hkv=2) == gqa.GQA_ERR_UNSUPPORTED         # G = 16 > 8
+    assert _dec8(lib, ns=2) == gqa.GQA_ERR_INVALID_ARG                 # two splits need a workspace

@@ -422,3 +422,38 @@ def test_varlen_sequence_order_permutes_rows_exactly():
     a, b_ = run([0, 1, 2]), run([2, 0, 1])
     for s in range(3):
         assert np.array_equal(a[s][0], b_[s][0]) and np.array_equal(a[s][1], b_[s][1])
+
+
+# ------------------------------------------------------------ FP8 KV decode
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_fp8_decode_oracle_matches_brute_force_on_dequantised_values(seed):
+    # brute force on k_scale * k8 and v_scale * v8 formed exactly in fp64:
+    # pins the folding of k_scale into the softmax scale and v_scale into out
+    d = inputs.make_decode_fp8(2, 4, 2, 8, 9, seed=seed, lens=(0, 9))
+    out, lse = oracle.decode_fp8(d["q"], d["kcache"], d["vcache"], d["k_scale"], d["v_scale"],
+                                 d["cache_seqlens"], scale=0.3)
+    qf = d["q"].float().numpy().astype(np.float64)
+    kf = d["kcache"].float().numpy().astype(np.float64) * d["k_scale"]
+    vf = d["vcache"].float().numpy().astype(np.float64) * d["v_scale"]
+    lens = d["cache_seqlens"].tolist()
+    bo, bl = brute.attention(qf[:, None].tolist(), kf.tolist(), vf.tolist(), 0.3, False, lens)
+    np.testing.assert_allclose(out, np.array(bo)[:, 0], rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(lse, np.array(bl)[:, :, 0], rtol=1e-12, atol=1e-12)
+
+
+def test_fp8_decode_with_unit_scales_is_decode_on_the_e4m3_values():
+    d = inputs.make_decode_fp8(3, 8, 2, 16, 20, seed=4, lens=(1, 20))
+    a, la = oracle.decode_fp8(d["q"], d["kcache"], d["vcache"], 1.0, 1.0, d["cache_seqlens"], scale=0.25)
+    b, lb = oracle.decode(d["q"], d["kcache"].float(), d["vcache"].float(), d["cache_seqlens"], scale=0.25)
+    assert np.array_equal(a, b) and np.array_equal(la, lb)
+
+
+def test_e4m3_quantisation_is_finite_and_within_half_an_ulp():
+    x = torch.randn(4096, generator=torch.Generator().manual_seed(0)) * 3
+    x8, s = inputs.quantize_e4m3(x)
+    y = x8.float()
+    assert torch.isfinite(y).all() and float(y.abs().max()) == 448.0
+    # e4m3 keeps 3 mantissa bits: relative rounding error <= 2^-4 for normal values
+    rel = ((y * s - x).abs() / x.abs().clamp_min(1e-30))[x.abs() / s >= 2 ** -6]
+    assert float(rel.max()) <= 2 ** -4 + 1e-7
