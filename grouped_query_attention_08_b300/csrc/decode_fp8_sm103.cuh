@@ -49,7 +49,7 @@ struct ParamsF8 {
 // Per-warp ring of 16-key blocks, K rows then V rows, 128 bytes per row,
 // chunks XOR-swizzled with swz() as in the bf16 ring.
 struct RingF8 {
-  static constexpr int kRing = 6;                          // 5 blocks in flight per warp
+  static constexpr int kRing = 4;                          // 3 blocks in flight per warp, 3 CTAs per SM
   static constexpr uint32_t kRowBytes = kF8D;
   static constexpr uint32_t kSlotBytes = 2 * kBlockKeys * kRowBytes;
   static constexpr uint32_t kWarpBytes = kRing * kSlotBytes;
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const Params
     const int k0 = kstart + blk * kBlockKeys;
 
     // S^T = K . Q^T: k-step ks = 4 q + j uses raw word j of chunk c + 4q
-    float s[4] = {0.f, 0.f, 0.f, 0.f};
+    float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};   // two independent chains
 #pragma unroll
     for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -226,8 +226,13 @@ __global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const Params
         uint32_t a0, a2, a1, a3;
         e4m3x4_to_f16x2x2(word(cur.k[0][q], j), a0, a2);
         e4m3x4_to_f16x2x2(word(cur.k[1][q], j), a1, a3);
-        mma_f16_16816(s, a0, a1, a2, a3, qf[4 * q + j][0], qf[4 * q + j][1]);
+        if (j & 1)
+          mma_f16_16816(s2, a0, a1, a2, a3, qf[4 * q + j][0], qf[4 * q + j][1]);
+        else
+          mma_f16_16816(s, a0, a1, a2, a3, qf[4 * q + j][0], qf[4 * q + j][1]);
       }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[e] += s2[e];
     const bool v0 = (k0 + r) < kend, v1 = (k0 + r + 8) < kend;
     const float tA0 = v0 ? s[0] * cl : -INFINITY, tB0 = v0 ? s[1] * cl : -INFINITY;
     const float tA1 = v1 ? s[2] * cl : -INFINITY, tB1 = v1 ? s[3] * cl : -INFINITY;
