@@ -173,3 +173,47 @@ def decode_fp8(q, kcache8, vcache8, k_scale, v_scale, cache_seqlens, *, scale=No
         scale = 1.0 / math.sqrt(q.shape[-1])
     out, lse = decode(q, f8(kcache8), f8(vcache8), cache_seqlens, scale=float(scale) * float(k_scale), rows=rows)
     return out * float(v_scale), lse
+
+
+def attention_blockmask(q, k, v, block_mask, block_size, *, scale=None, causal=False, seqlens_k=None):
+    """Oracle GQA attention with a block-sparsity mask ([GQA-BERT] "阶段二":
+    block_size, sparse=True; the pattern is the caller's).
+
+    q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D]; block_mask [ceil(Sq/bs), ceil(Sk/bs)] (nonzero =
+    attend), shared by every batch entry and head.  Key j is admissible for query i
+    when j < L_b, (not causal or j <= i + Sk - Sq) and block_mask[i//bs][j//bs] != 0.
+    Plain definition per (b, h) in fp64: scores by one matrix product, excluded keys
+    dropped, softmax against the row maximum.  Returns out [B,Sq,Hq,D], lse [B,Hq,Sq].
+    """
+    q, k, v = _f32(q).astype(np.float64), _f32(k).astype(np.float64), _f32(v).astype(np.float64)
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    bm = np.asarray(block_mask.cpu().numpy() if hasattr(block_mask, "cpu") else block_mask) != 0
+    bs = int(block_size)
+    if bm.shape != ((Sq + bs - 1) // bs, (Sk + bs - 1) // bs):
+        raise ValueError("block_mask must be [ceil(Sq/bs), ceil(Sk/bs)]")
+    lens = None if seqlens_k is None else np.asarray(
+        seqlens_k.cpu().numpy() if hasattr(seqlens_k, "cpu") else seqlens_k).astype(np.int64)
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
+    base = bm[i // bs, j // bs]
+    if causal:
+        base = base & (j <= i + Sk - Sq)
+    out = np.zeros((B, Sq, Hq, D), np.float64)
+    lse = np.full((B, Hq, Sq), -np.inf, np.float64)
+    for b in range(B):
+        allowed = base & (j < (Sk if lens is None else lens[b]))
+        any_key = allowed.any(axis=1)
+        for h in range(Hq):
+            s = scale * (q[b, :, h, :] @ k[b, :, h // G, :].T)
+            s = np.where(allowed, s, -np.inf)
+            m = np.where(any_key, s.max(axis=1), 0.0)
+            w = np.where(allowed, np.exp(s - m[:, None]), 0.0)
+            l = w.sum(axis=1)
+            ok = l > 0
+            out[b, ok, h, :] = (w[ok] / l[ok, None]) @ v[b, :, h // G, :]
+            lse[b, h, ok] = m[ok] + np.log(l[ok])
+    return out, lse

@@ -93,3 +93,31 @@ def attention_packed(q, k, v, cu_q, cu_k, scale, causal=False):
                     out[r][h][d] = math.fsum(w / total * v[kr][g][d] for w, kr in zip(weights, rows))
                 lse[h][r] = top + math.log(total)
     return out, lse
+
+
+def attention_blockmask(q, k, v, scale, block_mask, block_size, causal=False, seqlens_k=None):
+    """``attention`` restricted by a block mask: key j is a candidate for query
+    i only when block_mask[i // block_size][j // block_size] is nonzero (in
+    addition to the key length and the causal condition)."""
+    B, Sq, Sk = len(q), len(q[0]), len(k[0])
+    Hq, D, Hkv = len(q[0][0]), len(q[0][0][0]), len(k[0][0])
+    group = Hq // Hkv
+    out = [[[[0.0] * D for _ in range(Hq)] for _ in range(Sq)] for _ in range(B)]
+    lse = [[[-math.inf] * Sq for _ in range(Hq)] for _ in range(B)]
+    for b in range(B):
+        length = Sk if seqlens_k is None else int(seqlens_k[b])
+        for i in range(Sq):
+            keys = [j for j in range(length) if ((not causal) or j <= i + Sk - Sq)
+                    and block_mask[i // block_size][j // block_size]]
+            if not keys:
+                continue
+            for h in range(Hq):
+                g = h // group
+                scores = [scale * math.fsum(q[b][i][h][d] * k[b][j][g][d] for d in range(D)) for j in keys]
+                top = max(scores)
+                weights = [math.exp(s - top) for s in scores]
+                total = math.fsum(weights)
+                for d in range(D):
+                    out[b][i][h][d] = math.fsum(w / total * v[b][j][g][d] for w, j in zip(weights, keys))
+                lse[b][h][i] = top + math.log(total)
+    return out, lse

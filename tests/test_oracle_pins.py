@@ -457,3 +457,63 @@ def test_e4m3_quantisation_is_finite_and_within_half_an_ulp():
     # e4m3 keeps 3 mantissa bits: relative rounding error <= 2^-4 for normal values
     rel = ((y * s - x).abs() / x.abs().clamp_min(1e-30))[x.abs() / s >= 2 ** -6]
     assert float(rel.max()) <= 2 ** -4 + 1e-7
+
+
+# ------------------------------------------------------------ block-sparse
+
+def _bm_cases(n, seed):
+    rng = random.Random(seed)
+    out = []
+    for _ in range(n):
+        bs = rng.choice([1, 2, 4])
+        Sq, Sk = rng.randint(1, 13), rng.randint(1, 13)
+        Hkv = rng.choice([1, 2])
+        out.append((rng.choice([1, 2]), Hkv * rng.choice([1, 2, 3]), Hkv, Sq, Sk, rng.choice([1, 4]), bs,
+                    rng.random() < 0.5, rng.random() < 0.5, rng.choice([0.4, -0.8]), rng.randint(0, 1 << 30)))
+    return out
+
+
+@pytest.mark.parametrize("case", _bm_cases(60, 4242))
+def test_blockmask_oracle_matches_brute_force(case):
+    B, Hq, Hkv, Sq, Sk, D, bs, causal, padded, scale, seed = case
+    rng = np.random.default_rng(seed)
+    q, k, v = _rand((B, Sq, Hq, D), rng), _rand((B, Sk, Hkv, D), rng), _rand((B, Sk, Hkv, D), rng)
+    bm = (rng.random(((Sq + bs - 1) // bs, (Sk + bs - 1) // bs)) < 0.6).astype(np.uint8)
+    lens = [int(x) for x in rng.integers(0, Sk + 1, B)] if padded else None
+    out, lse = oracle.attention_blockmask(q, k, v, bm, bs, scale=scale, causal=causal, seqlens_k=lens)
+    bo, bl = brute.attention_blockmask(_tolist(q), _tolist(k), _tolist(v), scale, bm.tolist(), bs, causal, lens)
+    np.testing.assert_allclose(out, np.array(bo), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, np.array(bl), rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_blockmask_all_ones_is_the_dense_oracle(causal):
+    rng = np.random.default_rng(1)
+    q, k, v = _rand((2, 50, 8, 16), rng), _rand((2, 70, 2, 16), rng), _rand((2, 70, 2, 16), rng)
+    lens = np.array([70, 33], np.int32)
+    bm = np.ones(((50 + 63) // 64, (70 + 63) // 64), np.uint8)
+    a, la = oracle.attention_blockmask(q, k, v, bm, 64, scale=0.2, causal=causal, seqlens_k=lens)
+    b, lb = oracle.attention(q, k, v, scale=0.2, causal=causal, seqlens_k=lens)
+    np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(la, lb, rtol=1e-12, atol=1e-12)
+
+
+def test_block_diagonal_mask_is_separate_attention_per_segment():
+    # with only the diagonal blocks kept, each segment of bs queries attends to
+    # its own bs keys: the dense oracle on that segment alone
+    rng = np.random.default_rng(2)
+    bs, nb = 4, 3
+    q, k, v = _rand((1, bs * nb, 4, 8), rng), _rand((1, bs * nb, 2, 8), rng), _rand((1, bs * nb, 2, 8), rng)
+    out, lse = oracle.attention_blockmask(q, k, v, np.eye(nb, dtype=np.uint8), bs, scale=0.5)
+    for s in range(nb):
+        sl = slice(s * bs, (s + 1) * bs)
+        o, l = oracle.attention(q[:, sl], k[:, sl], v[:, sl], scale=0.5)
+        np.testing.assert_allclose(out[:, sl], o, rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(lse[:, :, sl], l, rtol=1e-12, atol=1e-12)
+
+
+def test_empty_block_mask_gives_zero_output_and_minus_inf_lse():
+    rng = np.random.default_rng(3)
+    q, k, v = _rand((1, 5, 2, 4), rng), _rand((1, 6, 1, 4), rng), _rand((1, 6, 1, 4), rng)
+    out, lse = oracle.attention_blockmask(q, k, v, np.zeros((1, 1), np.uint8), 8)
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
