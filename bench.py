@@ -255,7 +255,17 @@ def time_prefill_workload(gqa, name, device, flush, reps=10, warmup=3):
     inp = inputs.make_workload(w)
     d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
     out = torch.empty_like(d["q"])
-    if isinstance(w, inputs.VarlenWorkload):
+    if isinstance(w, inputs.SparseWorkload):
+        base = inputs.WORKLOADS[w.base]
+        lens = None if inp["seqlens_k"] is None else inp["seqlens_k"].tolist()
+        flops = 4 * base.D * roofline.blockmask_pairs(base.B, base.Hq, base.Sq, base.Sk, base.causal,
+                                                      inp["block_mask"], w.block_size, lens)
+        lse = torch.empty((base.B, base.Hq, base.Sq), dtype=torch.float32, device=device)
+
+        def call():
+            gqa.gqa_fwd_sparse(d["q"], d["k"], d["v"], d["block_mask"], w.block_size, causal=base.causal,
+                               seqlens_k=d["seqlens_k"], scale=base.scale, out=out, lse=lse)
+    elif isinstance(w, inputs.VarlenWorkload):
         # packed sequences: only real (query, key) pairs are work
         lq = (inp["cu_seqlens_q"][1:] - inp["cu_seqlens_q"][:-1]).tolist()
         lk = (inp["cu_seqlens_k"][1:] - inp["cu_seqlens_k"][:-1]).tolist()
@@ -325,6 +335,9 @@ def time_decode_fp8(gqa, name, device, flush, reps=20, warmup=3):
 
 
 def _workload_name(w):
+    if isinstance(w, inputs.SparseWorkload):
+        return "%s: %s under a block mask, %d-token blocks, band of +-%d blocks plus key block 0" % (
+            w.name, _workload_name(inputs.WORKLOADS[w.base]), w.block_size, w.window)
     if isinstance(w, inputs.VarlenWorkload):
         return "%s packed prefill B%d Hq%d Hkv%d D%d %s lengths U[%d,%d] (queries = keys), no padding" % (
             w.name, w.B, w.Hq, w.Hkv, w.D, "causal" if w.causal else "non-causal", w.lens[0], w.lens[1])
@@ -489,7 +502,7 @@ def main():
     dec8 = None
     if not args.no_other_workloads:
         del P, pin, out_p, lse_p
-        for name in ("bert_base", "bert_large_long", "causal_long", "bert_base_varlen"):
+        for name in ("bert_base", "bert_large_long", "causal_long", "bert_base_varlen", "bert_large_long_sparse"):
             if name == args.prefill:
                 others[name] = {"tflops": value / ws, "ms": pre_avg * 1e3}
                 continue

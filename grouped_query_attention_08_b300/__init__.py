@@ -66,6 +66,9 @@ def load_library():
         lib.gqa_decode_fp8.restype = i32
         lib.gqa_decode_fp8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, f32, f32, i32, i32, vp, sz,
                                        vp]
+        lib.gqa_fwd_sparse.restype = i32
+        lib.gqa_fwd_sparse.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp,
+                                       i32, vp]
         lib.gqa_decode.restype = i32
         lib.gqa_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, vp, sz, vp]
         lib.gqa_decode_num_splits.restype = i32
@@ -204,6 +207,44 @@ def gqa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q=None, ma
                                        int(bool(causal)), code, _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_fwd_varlen")
+    return out, lse
+
+
+def gqa_fwd_sparse(q, k, v, block_mask, block_size, *, causal=False, seqlens_k=None, scale=None, out=None,
+                   lse=None, return_lse=True, stream=None):
+    """Block-sparse GQA attention.  q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D] (bf16 or fp32, CUDA);
+    block_mask uint8/bool CUDA tensor [ceil(Sq/bs), ceil(Sk/bs)] (nonzero = attend), shared
+    by all batch entries and heads; block_size 64 or 128.  Returns (out, lse) as gqa_fwd.
+    """
+    torch = _torch()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, S, H, D]")
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between q, k and v")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    code = _dtype_code(q)
+    bs = int(block_size)
+    if block_mask.dtype == torch.bool:
+        block_mask = block_mask.to(torch.uint8)
+    if block_mask.dtype != torch.uint8 or tuple(block_mask.shape) != ((Sq + bs - 1) // bs, (Sk + bs - 1) // bs):
+        raise ValueError("block_mask must be uint8 [ceil(Sq/bs), ceil(Sk/bs)]")
+    if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or tuple(seqlens_k.shape) != (B,)):
+        raise ValueError("seqlens_k must be int32 [B]")
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    dev = _check_cuda(q, k, v, out, lse, seqlens_k, block_mask)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = load_library().gqa_fwd_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(block_mask), bs,
+                                       B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)), _ptr(seqlens_k),
+                                       code, _stream(dev, stream))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_fwd_sparse")
     return out, lse
 
 

@@ -35,6 +35,10 @@ struct Params {
   const int* cu_q;
   const int* cu_k;
   int total_q, total_k;
+  // block sparsity (dense layout): key j is a candidate for query i only
+  // when bmask[(i / bs) * n_kb + j / bs] != 0
+  const uint8_t* bmask;
+  int bs, n_kb;
   long long q_sb, q_ss, q_sh;   // element strides of q/out: batch, token, head
   long long k_sb, k_ss, k_sh;   // element strides of k/v: batch, key, kv head
   int B, Hq, Hkv, G, Sq, Sk, D, causal;
@@ -105,7 +109,9 @@ __global__ void __launch_bounds__(kWarps * 32) attention_kernel(const Params p) 
   const float* kb = p.k + k_off + (long long)kvh * p.k_sh;
   const float* vb = p.v + k_off + (long long)kvh * p.k_sh;
   float m = -INFINITY, l = 0.f;
+  const uint8_t* mrow = p.bmask ? p.bmask + (size_t)(i / p.bs) * p.n_kb : nullptr;
   for (int j = j0; j < j1; ++j) {
+    if (mrow && !mrow[j / p.bs]) continue;
     const float* kr = kb + (long long)j * p.k_ss;
     float part = 0.f;
 #pragma unroll

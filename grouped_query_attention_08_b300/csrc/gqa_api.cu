@@ -123,8 +123,10 @@ bool prefill_smem_attr_set(int dev) {
   static_assert(2 * 128 * pf::kSoftmaxRegs + 128 * pf::kOtherRegs <= pf::kThreads * pf::kLaunchRegs,
                 "register split exceeds the launch budget");
   // both layouts: dense and packed
-  for (const void* fn : {reinterpret_cast<const void*>(pf::prefill_kernel<D, false>),
-                         reinterpret_cast<const void*>(pf::prefill_kernel<D, true>)}) {
+  // every layout: dense, packed, block-sparse
+  for (const void* fn : {reinterpret_cast<const void*>(pf::prefill_kernel<D, false, false>),
+                         reinterpret_cast<const void*>(pf::prefill_kernel<D, true, false>),
+                         reinterpret_cast<const void*>(pf::prefill_kernel<D, false, true>)}) {
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, fn) != cudaSuccess) return false;
     if (fa.numRegs != pf::kLaunchRegs) return false;
@@ -140,7 +142,8 @@ bool prefill_smem_attr_set(int dev) {
 template <int D>
 int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv,
                         int Sq, int Sk, float scale, int causal, const int* seqlens_k, const int* cu_q,
-                        const int* cu_k, int total_q, int total_k, cudaStream_t stream) {
+                        const int* cu_k, int total_q, int total_k, const uint8_t* bmask, int bs,
+                        cudaStream_t stream) {
   namespace pf = gqa::prefill;
   const int G = Hq / Hkv;
   const int Mq = pf::kBM / G;
@@ -170,6 +173,10 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   p.total_q = total_q;
   p.total_k = total_k;
   p.lse_stride = cu_q ? total_q : Sq;
+  p.bmask = bmask;
+  p.bs = bs;
+  p.n_qb = bmask ? (Sq + bs - 1) / bs : 0;
+  p.n_kb = bmask ? (Sk + bs - 1) / bs : 0;
   p.B = B;
   p.Hq = Hq;
   p.Hkv = Hkv;
@@ -184,11 +191,14 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.timeout_ns = wait_timeout_ns();
-  if (cu_q)
-    pf::prefill_kernel<D, true><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(tmQ, tmK, tmV,
+  if (bmask)
+    pf::prefill_kernel<D, false, true><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(
+        tmQ, tmK, tmV, tmO, p);
+  else if (cu_q)
+    pf::prefill_kernel<D, true, false><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(tmQ, tmK, tmV,
                                                                                                  tmO, p);
   else
-    pf::prefill_kernel<D, false><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(tmQ, tmK, tmV,
+    pf::prefill_kernel<D, false, false><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(tmQ, tmK, tmV,
                                                                                                   tmO, p);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
@@ -301,9 +311,9 @@ int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, 
     if (Hq / Hkv > gqa::prefill::kBM) return GQA_ERR_UNSUPPORTED;
     if ((long long)Hq * D * Sq * B > (1LL << 40)) return GQA_ERR_UNSUPPORTED;
     return D == 64 ? launch_prefill_bf16<64>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k,
-                                             nullptr, nullptr, 0, 0, st)
+                                             nullptr, nullptr, 0, 0, nullptr, 0, st)
                    : launch_prefill_bf16<128>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k,
-                                              nullptr, nullptr, 0, 0, st);
+                                              nullptr, nullptr, 0, 0, nullptr, 0, st);
   }
   if (dtype == GQA_DTYPE_FP32) {
     if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4)) return GQA_ERR_INVALID_ARG;
@@ -357,9 +367,11 @@ int gqa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float
     if ((long long)Hq * D * total_q > (1LL << 40) || (long long)Hkv * D * total_k > (1LL << 40))
       return GQA_ERR_UNSUPPORTED;
     return D == 64 ? launch_prefill_bf16<64>(q, k, v, out, lse, B, Hq, Hkv, max_seqlen_q, max_seqlen_k, scale,
-                                             causal, nullptr, cu_seqlens_q, cu_seqlens_k, total_q, total_k, st)
+                                             causal, nullptr, cu_seqlens_q, cu_seqlens_k, total_q, total_k,
+                                             nullptr, 0, st)
                    : launch_prefill_bf16<128>(q, k, v, out, lse, B, Hq, Hkv, max_seqlen_q, max_seqlen_k, scale,
-                                              causal, nullptr, cu_seqlens_q, cu_seqlens_k, total_q, total_k, st);
+                                              causal, nullptr, cu_seqlens_q, cu_seqlens_k, total_q, total_k,
+                                              nullptr, 0, st);
   }
   if (dtype == GQA_DTYPE_FP32) {
     if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4)) return GQA_ERR_INVALID_ARG;
@@ -443,6 +455,64 @@ int gqa_decode_fp8(const void* q, const void* kcache, const void* vcache, const 
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
   }
   return GQA_OK;
+}
+
+int gqa_fwd_sparse(const void* q, const void* k, const void* v, void* out, float* lse, const unsigned char* block_mask,
+                   int block_size, int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+                   const int* seqlens_k, int dtype, void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return GQA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !block_mask) return GQA_ERR_INVALID_ARG;
+  if (block_size != 64 && block_size != 128) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
+  if ((lse && !aligned(lse, 4)) || (seqlens_k && !aligned(seqlens_k, 4))) return GQA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == GQA_DTYPE_BF16) {
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return GQA_ERR_INVALID_ARG;
+    if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+    if (Hq / Hkv > gqa::prefill::kBM) return GQA_ERR_UNSUPPORTED;
+    if (Sk > 64 * gqa::prefill::kBN) return GQA_ERR_UNSUPPORTED;   // one 64-bit word of key tiles per unit
+    if ((long long)Hq * D * Sq * B > (1LL << 40)) return GQA_ERR_UNSUPPORTED;
+    return D == 64 ? launch_prefill_bf16<64>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k,
+                                             nullptr, nullptr, 0, 0, block_mask, block_size, st)
+                   : launch_prefill_bf16<128>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k,
+                                              nullptr, nullptr, 0, 0, block_mask, block_size, st);
+  }
+  if (dtype == GQA_DTYPE_FP32) {
+    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4)) return GQA_ERR_INVALID_ARG;
+    if (D > gqa::f32::kMaxD) return GQA_ERR_UNSUPPORTED;
+    gqa::f32::Params p{};
+    p.q = static_cast<const float*>(q);
+    p.k = static_cast<const float*>(k);
+    p.v = static_cast<const float*>(v);
+    p.out = static_cast<float*>(out);
+    p.lse = lse;
+    p.seqlens = seqlens_k;
+    p.bmask = block_mask;
+    p.bs = block_size;
+    p.n_kb = (Sk + block_size - 1) / block_size;
+    p.q_sb = (long long)Sq * Hq * D;
+    p.q_ss = (long long)Hq * D;
+    p.q_sh = D;
+    p.k_sb = (long long)Sk * Hkv * D;
+    p.k_ss = (long long)Hkv * D;
+    p.k_sh = D;
+    p.B = B;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.Sq = Sq;
+    p.Sk = Sk;
+    p.D = D;
+    p.causal = causal;
+    p.scale = scale;
+    p.nsplit = 1;
+    p.split_len = Sk;
+    p.len_cap = Sk;
+    return launch_f32(p, st);
+  }
+  return GQA_ERR_INVALID_ARG;
 }
 
 int gqa_decode_num_splits(int B, int Hkv, int max_seqlen_k, int num_splits) {

@@ -132,6 +132,11 @@ struct Params {
   const int* cu_k;
   int total_q, total_k;
   int lse_stride;         // Sq (dense) or total_q (packed)
+  // Block sparsity (dense layout): bmask [n_qb, n_kb] uint8, nonzero = query
+  // block i // bs may attend to key block j // bs; bs = 64 or 128 and
+  // Sk <= 8192 (one 64-bit word of 128-key tiles per unit).
+  const uint8_t* bmask;
+  int bs, n_qb, n_kb;
   int B, Hq, Hkv, G, Sq, Sk;
   int Mq;                 // tokens per Q tile (G * Mq <= 128)
   int n_qblk;             // ceil(Sq / (kNQT * Mq))
@@ -152,6 +157,7 @@ struct Unit {
   int tb;                  // batch coordinate of the tensor maps (b, or 0 when packed)
   int diag;                // causal: query row i sees keys j <= i + diag
   bool has_rows;           // the unit holds at least one query row
+  uint64_t act;            // block sparsity: active 128-key tiles (n_tiles = their count)
   bool bad_len;
 };
 
@@ -159,7 +165,61 @@ struct Unit {
 // warp one unit ahead and passed on through the unit queue.
 struct SeqInfo {
   int Lk, Lq, qbase, kbase;
+  uint32_t act_lo, act_hi;   // block sparsity: the unit's active 128-key tiles
 };
+
+// One bit per byte of w: bit e set when byte e is nonzero.
+DEVI uint32_t nonzero_bytes4(uint32_t w) {
+  uint32_t t = w | (w >> 4);
+  t |= t >> 2;
+  t |= t >> 1;
+  return (t & 1u) | ((t >> 7) & 2u) | ((t >> 14) & 4u) | ((t >> 21) & 8u);
+}
+
+// Bits of row qb of the block mask: bit kb set when block (qb, kb) is kept.
+// Whole 16-byte chunks of the row by vector loads when the row is 16-byte
+// aligned, the rest byte by byte; nothing past the row is read.
+DEVI void mask_row_bits(const Params& p, int qb, uint64_t& lo, uint64_t& hi) {
+  lo = 0;
+  hi = 0;
+  const uint8_t* row = p.bmask + size_t(qb) * p.n_kb;
+  int kb = 0;
+  if ((reinterpret_cast<uintptr_t>(row) & 15u) == 0) {
+    for (; kb + 16 <= p.n_kb; kb += 16) {
+      uint4 w;
+      asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+                   : "l"(row + kb));
+      const uint64_t bits = uint64_t(nonzero_bytes4(w.x)) | (uint64_t(nonzero_bytes4(w.y)) << 4) |
+                            (uint64_t(nonzero_bytes4(w.z)) << 8) | (uint64_t(nonzero_bytes4(w.w)) << 12);
+      if (kb < 64) lo |= bits << kb; else hi |= bits << (kb - 64);
+    }
+  }
+  for (; kb < p.n_kb; ++kb) {
+    const uint64_t bit = row[kb] ? 1ull : 0ull;
+    if (kb < 64) lo |= bit << kb; else hi |= bit << (kb - 64);
+  }
+}
+
+// The 32 bits of x at even positions, packed (bit 2k -> bit k).
+DEVI uint64_t even_bits(uint64_t x) {
+  x &= 0x5555555555555555ull;
+  x = (x | (x >> 1)) & 0x3333333333333333ull;
+  x = (x | (x >> 2)) & 0x0F0F0F0F0F0F0F0Full;
+  x = (x | (x >> 4)) & 0x00FF00FF00FF00FFull;
+  x = (x | (x >> 8)) & 0x0000FFFF0000FFFFull;
+  x = (x | (x >> 16)) & 0x00000000FFFFFFFFull;
+  return x;
+}
+
+// Key-block bits (lo: blocks 0-63, hi: 64-127) -> 128-key-tile bits.  With
+// bs = 128 a tile is one block; with bs = 64 tile j holds blocks 2j (`half`
+// 0) and 2j+1 (`half` 1).
+DEVI uint64_t tiles_of_blocks(int bs, uint64_t lo, uint64_t hi, int half) {
+  if (bs == 128) return lo;
+  const uint64_t a = half ? lo >> 1 : lo, b = half ? hi >> 1 : hi;
+  return even_bits(a) | (even_bits(b) << 32);
+}
 
 // Position of work unit u = qidx * (B * Hkv) + b * Hkv + kvh.
 struct UnitPos {
@@ -212,7 +272,7 @@ DEVI int claim_unit(const Params& p) {
 
 // Work unit -> (b, kvh, first token, key length, number of key tiles); len is
 // unit_len of the same unit.
-template <bool kPacked>
+template <bool kPacked, bool kSparse>
 DEVI Unit unit_info(const Params& p, const UnitPos& x, const SeqInfo& sq) {
   Unit U;
   const int qblk = p.causal ? p.n_qblk - 1 - x.qidx : x.qidx;   // causal: longest units first
@@ -243,10 +303,31 @@ DEVI Unit unit_info(const Params& p, const UnitPos& x, const SeqInfo& sq) {
   int kmax = Lb;
   if (p.causal) kmax = min(kmax, q_last + U.diag + 1);
   U.n_tiles = (U.has_rows && kmax > 0) ? (kmax + kBN - 1) / kBN : 0;
+  if constexpr (kSparse) {
+    // the tiles within reach (n_tiles <= 64: Sk <= 8192) that a block of the
+    // unit's rows keeps; n_tiles becomes their count
+    const uint64_t reach = U.n_tiles >= 64 ? ~0ull : ((1ull << U.n_tiles) - 1);
+    U.act = ((uint64_t(sq.act_hi) << 32) | sq.act_lo) & reach;
+    U.n_tiles = __popcll(U.act);
+  }
   return U;
 }
 
-template <int D, bool kPacked>
+// Block sparsity: the 128-key tiles that any query block of the unit keeps
+// (U is the unit's dense geometry).
+DEVI uint64_t unit_active_tiles(const Params& p, const Unit& U) {
+  if (!U.has_rows || U.n_tiles == 0) return 0;
+  const int q_last = min(U.q0 + kNQT * p.Mq, U.Lq) - 1;
+  uint64_t act = 0;
+  for (int qb = U.q0 / p.bs; qb <= q_last / p.bs; ++qb) {
+    uint64_t lo, hi;
+    mask_row_bits(p, qb, lo, hi);
+    act |= tiles_of_blocks(p.bs, lo, hi, 0) | tiles_of_blocks(p.bs, lo, hi, 1);
+  }
+  return act;
+}
+
+template <int D, bool kPacked, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
@@ -302,6 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         sq.Lq = uq[8 * i + 2];
         sq.qbase = uq[8 * i + 3];
         sq.kbase = uq[8 * i + 4];
+      }
+      if constexpr (kSparse) {
+        sq.act_lo = uint32_t(uq[8 * i + 5]);
+        sq.act_hi = uint32_t(uq[8 * i + 6]);
       }
     }
     if (whole_warp) {
@@ -383,15 +468,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const UnitPos x = upos_of(p, u < p.n_units ? u : 0);
         SeqInfo sq{0, 0, 0, 0};
         if (u < p.n_units) sq = unit_seq<kPacked>(p, x);
+        if constexpr (kSparse) {
+          if (u < p.n_units) {
+            const uint64_t act = unit_active_tiles(p, unit_info<kPacked, false>(p, x, sq));
+            sq.act_lo = uint32_t(act);
+            sq.act_hi = uint32_t(act >> 32);
+          }
+        }
         if (u < p.n_units) u_next = claim_unit(p);
         uq[8 * i] = u;
         uq[8 * i + 1] = sq.Lk;
         uq[8 * i + 2] = sq.Lq;
         uq[8 * i + 3] = sq.qbase;
         uq[8 * i + 4] = sq.kbase;
+        if constexpr (kSparse) {
+          uq[8 * i + 5] = int(sq.act_lo);
+          uq[8 * i + 6] = int(sq.act_hi);
+        }
         mbar_arrive(uq_full(i));        // release: the entry is visible to the consumers
         if (u >= p.n_units) break;
-        const Unit U = unit_info<kPacked>(p, x, sq);
+        const Unit U = unit_info<kPacked, kSparse>(p, x, sq);
         if (U.bad_len) raise_error(kErrBounds);
         if (U.n_tiles == 0) continue;
         const int qb = int(qn % QB);
@@ -403,7 +499,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(base + L::kOffQ + qb * L::kQSetBytes + t * L::kTileBytes + h * L::kHalfBytes, &tmQ,
                         q_full(qb), h * 64, U.kvh * p.G, U.qbase + U.q0 + t * p.Mq, U.tb);
         ++qn;
+        uint64_t act_rem = kSparse ? U.act : 0ull;     // block sparsity: active tiles still to load
         for (int j = 0; j < U.n_tiles; ++j) {
+          int tj = j;                  // key tile index (the j-th active tile when sparse)
+          if constexpr (kSparse) {
+            tj = __ffsll((long long)act_rem) - 1;
+            act_rem &= act_rem - 1;
+          }
           const int s = int(kv_it % S);
           const uint32_t ph = (kv_it / S) & 1;
           ok = mbar_wait(k_empty(s), ph ^ 1, abort_flag, to);
@@ -411,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(k_full(s), L::kTileBytes);
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_4d(base + L::kOffK + s * L::kTileBytes + h * L::kHalfBytes, &tmK, k_full(s), h * 64,
-                        U.kvh, U.kbase + j * kBN, U.tb);
+                        U.kvh, U.kbase + tj * kBN, U.tb);
           ok = mbar_wait(v_empty(s), ph ^ 1, abort_flag, to);
           if (!ok) {
             k_only = true;     // K of ring position kv_it is in flight, V is not
@@ -420,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(v_full(s), L::kTileBytes);
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_4d(base + L::kOffV + s * L::kTileBytes + h * L::kHalfBytes, &tmV, v_full(s), h * 64,
-                        U.kvh, U.kbase + j * kBN, U.tb);
+                        U.kvh, U.kbase + tj * kBN, U.tb);
           ++kv_it;
         }
       }
@@ -493,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         SeqInfo sq;
         const int u = next_unit(k, sq, ok, false);
         if (!ok || u >= p.n_units) break;
-        const Unit U = unit_info<kPacked>(p, upos_of(p, u), sq);
+        const Unit U = unit_info<kPacked, kSparse>(p, upos_of(p, u), sq);
         const int n = U.n_tiles;
         if (n == 0) continue;
         const int qb = int(qn % QB);
@@ -606,7 +708,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if (u >= p.n_units) break;
-      const Unit U = unit_info<kPacked>(p, upos_of(p, u), sq);
+      const Unit U = unit_info<kPacked, kSparse>(p, upos_of(p, u), sq);
       const int token = U.q0 + t * p.Mq + r_tok;
       const bool row_ok = (r < rows_per_tile) && (token < U.Lq);
       int limit = 0;
@@ -619,6 +721,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       float l = 0.f;
 
       const int n = U.n_tiles;
+      // block sparsity: the unit's active tiles still to process, and the
+      // tiles this row's query block keeps for its low / high 64 keys
+      uint64_t act_rem = kSparse ? U.act : 0ull, row_lo = ~0ull, row_hi = ~0ull;
+      if constexpr (kSparse) {
+        if (row_ok) {
+          uint64_t blo, bhi;
+          mask_row_bits(p, token / p.bs, blo, bhi);
+          row_lo = tiles_of_blocks(p.bs, blo, bhi, 0);
+          row_hi = tiles_of_blocks(p.bs, blo, bhi, 1);
+        }
+      }
       uint32_t sv[kBN];        // S_t of the current key tile, in registers
       if (n > 0) {
         // S_t(0), read before the loop so that every tile's S is visibly
@@ -663,13 +776,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           return okn;
         };
 
-        const int lim = limit - j * kBN;
+        int tj = j;             // key tile index (the j-th active tile when sparse)
+        if constexpr (kSparse) {
+          tj = __ffsll((long long)act_rem) - 1;
+          act_rem &= act_rem - 1;
+        }
+        const int lim = limit - tj * kBN;
+        bool ok_lo = true, ok_hi = true;   // this row keeps the tile's low / high 64 keys
+        if constexpr (kSparse) {
+          ok_lo = (row_lo >> tj) & 1ull;
+          ok_hi = (row_hi >> tj) & 1ull;
+        }
         // Keys at or past the row's limit get exactly zero weight.  When every
         // row of the warp admits every key of the tile (rows that hold no
         // query are never stored and do not count) and the scale is positive,
         // no mask is needed and the max is taken on the raw scores.  Every
         // branch below is warp-uniform.
-        const bool full = __all_sync(0xffffffffu, lim >= kBN || !row_ok) && (c > 0.f);
+        const bool full = __all_sync(0xffffffffu, (lim >= kBN && ok_lo && ok_hi) || !row_ok) && (c > 0.f);
         float mt = -INFINITY;
         if (full) {
 #pragma unroll
@@ -678,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else {
 #pragma unroll
           for (int i = 0; i < kBN; ++i) {
-            const float f = (i < lim) ? __uint_as_float(sv[i]) * c : -INFINITY;
+            const float f = (i < lim && (i < 64 ? ok_lo : ok_hi)) ? __uint_as_float(sv[i]) * c : -INFINITY;
             sv[i] = __float_as_uint(f);
             mt = fmaxf(mt, f);
           }

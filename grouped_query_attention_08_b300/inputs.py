@@ -78,6 +78,15 @@ class VarlenWorkload:
         return 1.0 / math.sqrt(self.D)
 
 
+@dataclasses.dataclass(frozen=True)
+class SparseWorkload:
+    name: str
+    base: str                        # the dense workload whose inputs are used
+    block_size: int
+    pattern: str                     # "band": |qb - kb| <= window, plus key block 0
+    window: int
+
+
 WORKLOADS = {
     # tiny fp32 check case: B=1 Hq=4 Hkv=2 S=64 D=64, no padding
     "tiny": PrefillWorkload("tiny", 1, 4, 2, 64, 64, 64, False, None, "fp32", 0),
@@ -97,6 +106,9 @@ WORKLOADS = {
     "llama_decode_fp8": DecodeWorkload("llama_decode_fp8", 64, 64, 8, 128, 8192, (1024, 8192), "fp8kv", 3),
     "llama_decode_fp8_small": DecodeWorkload("llama_decode_fp8_small", 16, 64, 8, 128, 8192, (1024, 8192),
                                              "fp8kv", 3),
+    # bert_large_long under a block-sparse band: 128-token blocks, a window of
+    # +-2 blocks plus the first key block (global tokens), ~18 % of the blocks
+    "bert_large_long_sparse": SparseWorkload("bert_large_long_sparse", "bert_large_long", 128, "band", 2),
     # bert_base's batch packed without padding: each sequence's query and key
     # length ~ U[512,1024]
     "bert_base_varlen": VarlenWorkload("bert_base_varlen", 32, 12, 3, 64, False, (512, 1024), "bf16", 1),
@@ -195,10 +207,42 @@ def make_decode_fp8(B, Hq, Hkv, D, Smax, *, seed=0, lens=(1, None), q_mult=1.0):
                 cache_seqlens=d["cache_seqlens"])
 
 
+def make_block_mask(n_qb, n_kb, pattern="band", window=2, density=0.5, seed=0):
+    """uint8 [n_qb, n_kb] block mask: "band" keeps |qb - kb| <= window (query and key
+    blocks aligned at their starts) plus key block 0; "random" keeps each block with
+    probability ``density``; "ones" keeps all, "zeros" none."""
+    if pattern == "band":
+        qb = torch.arange(n_qb)[:, None]
+        kb = torch.arange(n_kb)[None, :]
+        m = ((qb - kb).abs() <= window) | (kb == 0)
+    elif pattern == "random":
+        g = torch.Generator("cpu").manual_seed(int(seed))
+        m = torch.rand((n_qb, n_kb), generator=g) < float(density)
+    elif pattern == "ones":
+        m = torch.ones((n_qb, n_kb), dtype=torch.bool)
+    elif pattern == "zeros":
+        m = torch.zeros((n_qb, n_kb), dtype=torch.bool)
+    else:
+        raise ValueError("unknown pattern %r" % pattern)
+    return m.to(torch.uint8)
+
+
+def make_sparse_workload(w):
+    """Inputs of a SparseWorkload: its base workload's tensors plus block_mask."""
+    base = WORKLOADS[w.base]
+    d = make_prefill(base.B, base.Hq, base.Hkv, base.Sq, base.Sk, base.D, seed=base.seed, lens=base.lens,
+                     dtype=base.dtype)
+    bs = w.block_size
+    d["block_mask"] = make_block_mask((base.Sq + bs - 1) // bs, (base.Sk + bs - 1) // bs, w.pattern, w.window)
+    return d
+
+
 def make_workload(w, seed=None):
     """Inputs of a named workload (a key of WORKLOADS or a workload object)."""
     if isinstance(w, str):
         w = WORKLOADS[w]
+    if isinstance(w, SparseWorkload):
+        return make_sparse_workload(w)
     s = w.seed if seed is None else seed
     if isinstance(w, DecodeWorkload) and w.dtype == "fp8kv":
         return make_decode_fp8(w.B, w.Hq, w.Hkv, w.D, w.Smax, seed=s, lens=w.lens)

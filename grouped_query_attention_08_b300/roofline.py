@@ -53,6 +53,27 @@ def prefill_flops(B, Hq, Sq, Sk, D, causal, seqlens_k=None) -> int:
     return 4 * D * prefill_pairs(B, Hq, Sq, Sk, causal, seqlens_k)
 
 
+def blockmask_pairs(B: int, Hq: int, Sq: int, Sk: int, causal: bool, block_mask, block_size: int,
+                    seqlens_k: Optional[Sequence[int]] = None) -> int:
+    """Admissible (b, h, i, j) pairs under a block mask [ceil(Sq/bs), ceil(Sk/bs)]
+    (nonzero = kept), the key lengths and the causal condition."""
+    bs = int(block_size)
+    rows = [[int(x) != 0 for x in r] for r in (block_mask.tolist() if hasattr(block_mask, "tolist")
+                                                 else block_mask)]
+    total = 0
+    for b in range(B):
+        Lb = Sk if seqlens_k is None else int(seqlens_k[b])
+        for i in range(Sq):
+            lim = min(Lb, i + Sk - Sq + 1) if causal else Lb
+            if lim <= 0:
+                continue
+            kept = rows[i // bs]
+            for kb in range((lim + bs - 1) // bs):
+                if kept[kb]:
+                    total += min(lim, (kb + 1) * bs) - kb * bs
+    return total * Hq
+
+
 def varlen_pairs(Hq: int, lens_q: Sequence[int], lens_k: Sequence[int], causal: bool) -> int:
     """Admissible (sequence, h, i, j) pairs of packed sequences; causal is
     bottom-right aligned per sequence (j <= i + Lk - Lq)."""

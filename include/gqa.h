@@ -136,6 +136,27 @@ int gqa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float
                    float scale, int causal, int dtype, void* stream);
 
 /*
+ * gqa_fwd_sparse -- gqa_fwd restricted by a block-sparsity mask ([GQA-BERT]
+ * "阶段二": block_size and sparse=True; the pages do not state the pattern,
+ * so it is the caller's).  Key blocks that no query of a work unit keeps are
+ * skipped (never loaded, never multiplied).
+ *
+ *   block_mask  uint8 [ceil(Sq/bs), ceil(Sk/bs)] device, row-major; nonzero
+ *               = the queries of block i // bs may attend to the keys of
+ *               block j // bs.  Shared by every batch entry and head.
+ *   block_size  bs, 64 or 128 (GQA_ERR_INVALID_ARG otherwise)
+ *   everything else as gqa_fwd (dense layout, seqlens_k, causal, lse).
+ * Key j is admissible for query i when j < L_b, the causal condition holds
+ * (if causal) and block_mask[i/bs][j/bs] != 0; rows with no admissible key
+ * give out = 0 and lse = -inf.  bf16: Sk <= 8192 (GQA_ERR_UNSUPPORTED
+ * otherwise), D 64 or 128, G <= 128.  fp32: as gqa_fwd.
+ */
+int gqa_fwd_sparse(const void* q, const void* k, const void* v, void* out, float* lse,
+                   const unsigned char* block_mask, int block_size, int B, int Hq, int Hkv,
+                   int Sq, int Sk, int D, float scale, int causal, const int* seqlens_k,
+                   int dtype, void* stream);
+
+/*
  * gqa_decode_num_splits -- the number of KV-length splits gqa_decode will use.
  * num_splits in 1..128 is returned clamped to the number of 16-key blocks of
  * max_seqlen_k; num_splits <= 0 asks for the automatic choice, which sizes

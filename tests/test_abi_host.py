@@ -152,3 +152,20 @@ def test_decode_fp8_validation(lib):
     assert _dec8(lib, D=64) == gqa.GQA_ERR_UNSUPPORTED                 # head dimension 128 only
     assert _dec8(lib, Hq=32, Hkv=2) == gqa.GQA_ERR_UNSUPPORTED         # G = 16 > 8
     assert _dec8(lib, ns=2) == gqa.GQA_ERR_INVALID_ARG                 # two splits need a workspace
+
+
+def _sparse(lib, B=1, Hq=4, Hkv=2, Sq=8, Sk=8, D=64, bs=64, scale=0.125, causal=0, dtype=0, q=FAKE, bm=FAKE):
+    P = ctypes.c_void_p
+    return lib.gqa_fwd_sparse(P(q), P(FAKE), P(FAKE), P(FAKE), None, P(bm) if bm else None, bs, B, Hq, Hkv, Sq,
+                              Sk, D, scale, causal, None, dtype, None)
+
+
+@pytest.mark.parametrize("kw", [dict(bm=0), dict(bs=32), dict(bs=100), dict(Hq=6, Hkv=4), dict(B=0),
+                                dict(scale=float("nan")), dict(causal=3), dict(q=FAKE + 8)])
+def test_fwd_sparse_rejects_invalid_arguments(lib, kw):
+    assert _sparse(lib, **kw) == gqa.GQA_ERR_INVALID_ARG
+
+
+def test_fwd_sparse_unsupported_shapes(lib):
+    assert _sparse(lib, Sk=8193) == gqa.GQA_ERR_UNSUPPORTED      # more than 64 key tiles of 128
+    assert _sparse(lib, D=96) == gqa.GQA_ERR_UNSUPPORTED
