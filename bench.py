@@ -45,8 +45,8 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # profiles/prefill_kernel_d64_bert_base.md (one launch, bert_base)
     "prefill": {"source": "grouped_query_attention_08_b300/csrc/prefill_sm103.cuh",
-                "sha256": "5ef35b9783edf6b9c32a946777bf59011fc0944f53dd5a00606698e03fb60c04",
-                "workload": "bert_base", "bytes": 94361088},
+                "sha256": "597407912e03c9d5f670a6fef6109fe8531859762cf0fdef7c02f64bd8cd5c42",
+                "workload": "bert_base", "bytes": 95083776},
     # profiles/decode_split_kernel_llama_decode_small.md (B=16 capture scaled to B=64 by KV bytes)
     "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh",
                "sha256": "bdbf5370ee5f9909a3c8113f1991ca09478653442bedf0c446fbd2db9b8c7ef8",
@@ -360,6 +360,11 @@ def main():
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip timing the other prefill workloads after the main run")
     ap.add_argument("--other-reps", type=int, default=10)
+    ap.add_argument("--other-workloads",
+                    default="bert_base,bert_large_long,causal_long,bert_base_varlen,bert_large_long_sparse,"
+                            "llama_decode_fp8",
+                    help="comma-separated workloads timed after the main run (FP8-cache decode workloads "
+                         "report under decode_fp8)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -502,12 +507,14 @@ def main():
     dec8 = None
     if not args.no_other_workloads:
         del P, pin, out_p, lse_p
-        for name in ("bert_base", "bert_large_long", "causal_long", "bert_base_varlen", "bert_large_long_sparse"):
-            if name == args.prefill:
+        for name in [n for n in args.other_workloads.split(",") if n]:
+            w = inputs.WORKLOADS[name]
+            if isinstance(w, inputs.DecodeWorkload) and w.dtype == "fp8kv":
+                dec8 = time_decode_fp8(gqa, name, device, flush, reps=max(args.other_reps, 1) * 2)
+            elif name == args.prefill:
                 others[name] = {"tflops": value / ws, "ms": pre_avg * 1e3}
-                continue
-            others[name] = time_prefill_workload(gqa, name, device, flush, reps=args.other_reps)
-        dec8 = time_decode_fp8(gqa, "llama_decode_fp8", device, flush)
+            else:
+                others[name] = time_prefill_workload(gqa, name, device, flush, reps=args.other_reps)
         torch.cuda.synchronize()
         if gqa.gqa_device_status() != 0:
             raise RuntimeError("device error while timing the other prefill workloads")
