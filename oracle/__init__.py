@@ -217,3 +217,49 @@ def attention_blockmask(q, k, v, block_mask, block_size, *, scale=None, causal=F
             out[b, ok, h, :] = (w[ok] / l[ok, None]) @ v[b, :, h // G, :]
             lse[b, h, ok] = m[ok] + np.log(l[ok])
     return out, lse
+
+
+def attention_backward(q, k, v, dout, *, scale=None, causal=False, seqlens_k=None):
+    """Oracle gradients of GQA attention (the forward's definition above) for an
+    upstream gradient dout [B,Sq,Hq,D].  Plain fp64 per (b, h) with P the exact
+    softmax over the admissible keys:
+        dV_j  += sum_i P_ij dO_i                 (summed over the G heads of the group)
+        dP_ij  = dO_i . v_j,   Dsum_i = sum_j P_ij dP_ij   (= dO_i . O_i)
+        dS_ij  = P_ij (dP_ij - Dsum_i)
+        dQ_i   = scale sum_j dS_ij k_j,   dK_j += scale sum_i dS_ij q_i
+    Returns dq [B,Sq,Hq,D], dk [B,Sk,Hkv,D], dv [B,Sk,Hkv,D] in float64.
+    """
+    q, k, v = (_f32(x).astype(np.float64) for x in (q, k, v))
+    do = _f32(dout).astype(np.float64)
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lens = None if seqlens_k is None else np.asarray(
+        seqlens_k.cpu().numpy() if hasattr(seqlens_k, "cpu") else seqlens_k).astype(np.int64)
+    i = np.arange(Sq)[:, None]
+    j = np.arange(Sk)[None, :]
+    dq = np.zeros_like(q)
+    dk = np.zeros((B, Sk, Hkv, D), np.float64)
+    dv = np.zeros((B, Sk, Hkv, D), np.float64)
+    for b in range(B):
+        allowed = j < (Sk if lens is None else lens[b])
+        if causal:
+            allowed = allowed & (j <= i + Sk - Sq)
+        any_key = allowed.any(axis=1)
+        for h in range(Hq):
+            g = h // G
+            s = scale * (q[b, :, h, :] @ k[b, :, g, :].T)
+            s = np.where(allowed, s, -np.inf)
+            m = np.where(any_key, s.max(axis=1), 0.0)
+            w = np.where(allowed, np.exp(s - m[:, None]), 0.0)
+            l = w.sum(axis=1)
+            p = np.where(any_key[:, None], w / np.where(l > 0, l, 1.0)[:, None], 0.0)
+            dp = do[b, :, h, :] @ v[b, :, g, :].T
+            dsum = (p * dp).sum(axis=1)
+            ds = p * (dp - dsum[:, None])
+            dq[b, :, h, :] = scale * (ds @ k[b, :, g, :])
+            dk[b, :, g, :] += scale * (ds.T @ q[b, :, h, :])
+            dv[b, :, g, :] += p.T @ do[b, :, h, :]
+    return dq, dk, dv

@@ -517,3 +517,64 @@ def test_empty_block_mask_gives_zero_output_and_minus_inf_lse():
     q, k, v = _rand((1, 5, 2, 4), rng), _rand((1, 6, 1, 4), rng), _rand((1, 6, 1, 4), rng)
     out, lse = oracle.attention_blockmask(q, k, v, np.zeros((1, 1), np.uint8), 8)
     assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+# ------------------------------------------------------------------ backward
+
+def _torch_reference_grads(q, k, v, do, scale, causal, lens):
+    # torch autograd in fp64 on the CPU (a library routine): GQA as MHA on K/V
+    # heads repeated per group, keys past the length or the diagonal masked
+    qt = torch.tensor(q, dtype=torch.float64, requires_grad=True)
+    kt = torch.tensor(k, dtype=torch.float64, requires_grad=True)
+    vt = torch.tensor(v, dtype=torch.float64, requires_grad=True)
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    kr = kt.repeat_interleave(G, dim=2).permute(0, 2, 3, 1)     # [B,Hq,D,Sk]
+    vr = vt.repeat_interleave(G, dim=2).permute(0, 2, 1, 3)     # [B,Hq,Sk,D]
+    s = scale * (qt.permute(0, 2, 1, 3) @ kr)                    # [B,Hq,Sq,Sk]
+    ii = torch.arange(Sq)[:, None]
+    jj = torch.arange(Sk)[None, :]
+    mask = torch.stack([(jj < (Sk if lens is None else lens[b])) & ((jj <= ii + Sk - Sq) if causal else True)
+                        for b in range(B)])[:, None]
+    s = s.masked_fill(~mask, float("-inf"))
+    out = torch.softmax(s, dim=-1) @ vr                          # [B,Hq,Sq,D]
+    out.permute(0, 2, 1, 3).backward(torch.tensor(do, dtype=torch.float64))
+    return qt.grad.numpy(), kt.grad.numpy(), vt.grad.numpy()
+
+
+@pytest.mark.parametrize("causal,lens", [(False, None), (True, None), (False, [5, 9])])
+def test_backward_oracle_matches_torch_autograd(causal, lens):
+    rng = np.random.default_rng(11)
+    B, Sq, Sk, Hq, Hkv, D = 2, 7, 9, 6, 2, 8
+    q, k, v = _rand((B, Sq, Hq, D), rng), _rand((B, Sk, Hkv, D), rng), _rand((B, Sk, Hkv, D), rng)
+    do = _rand((B, Sq, Hq, D), rng)
+    got = oracle.attention_backward(q, k, v, do, scale=0.4, causal=causal, seqlens_k=lens)
+    ref = _torch_reference_grads(q, k, v, do, 0.4, causal, lens)
+    for g, r in zip(got, ref):
+        np.testing.assert_allclose(g, r, rtol=1e-10, atol=1e-12)
+
+
+def test_backward_oracle_matches_central_differences():
+    # d<dO, out>/dx by central differences of the forward oracle (fp64)
+    rng = np.random.default_rng(12)
+    q, k, v = _rand((1, 3, 4, 2), rng), _rand((1, 4, 2, 2), rng), _rand((1, 4, 2, 2), rng)
+    do = _rand((1, 3, 4, 2), rng)
+    dq, dk, dv = oracle.attention_backward(q, k, v, do, scale=0.7, causal=True)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.attention(qq.astype(np.float32), kk.astype(np.float32), vv.astype(np.float32), scale=0.7,
+                                causal=True)
+        return float((o * do).sum())
+    def loss_with(which, x):
+        args = [q, k, v]
+        args[which] = x
+        return loss(*args)
+    eps = 1e-3
+    for which, (x, g) in enumerate(((q, dq), (k, dk), (v, dv))):
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            fd = (loss_with(which, xp) - loss_with(which, xm)) / (2 * eps)
+            assert abs(fd - g[idx]) <= 2e-4 * max(1.0, abs(g[idx])), (idx, fd, g[idx])
