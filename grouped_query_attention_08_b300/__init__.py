@@ -10,6 +10,10 @@ raise.
 Functions keep the C names:
   gqa_fwd(q, k, v, *, causal=False, seqlens_k=None, scale=None, out=None, lse=None, return_lse=True)
   gqa_decode(q, kcache, vcache, cache_seqlens, *, scale=None, num_splits=0, out=None, workspace=None)
+  gqa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *, causal=False, ...)
+  gqa_fwd_sparse(q, k, v, block_mask, block_size, *, causal=False, seqlens_k=None, ...)
+  gqa_bwd(q, k, v, out, dout, lse, *, causal=False, seqlens_k=None, scale=None, dq=None, dk=None, dv=None)
+  gqa_decode_fp8(q, kcache, vcache, cache_seqlens, *, k_scale, v_scale, ...)
   gqa_decode_num_splits(B, Hkv, max_seqlen_k, num_splits)
   gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, max_seqlen_k)
   gqa_device_status(stream=None)
@@ -69,6 +73,9 @@ def load_library():
         lib.gqa_fwd_sparse.restype = i32
         lib.gqa_fwd_sparse.argtypes = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, f32, i32, vp,
                                        i32, vp]
+        lib.gqa_bwd.restype = i32
+        lib.gqa_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32,
+                                vp, i32, vp]
         lib.gqa_decode.restype = i32
         lib.gqa_decode.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, vp, sz, vp]
         lib.gqa_decode_num_splits.restype = i32
@@ -246,6 +253,46 @@ def gqa_fwd_sparse(q, k, v, block_mask, block_size, *, causal=False, seqlens_k=N
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_fwd_sparse")
     return out, lse
+
+
+def gqa_bwd(q, k, v, out, dout, lse, *, causal=False, seqlens_k=None, scale=None, dq=None, dk=None, dv=None,
+            dsum=None, stream=None):
+    """Gradients of gqa_fwd.  q/out/dout [B,Sq,Hq,D], k/v [B,Sk,Hkv,D] bf16 CUDA; lse fp32
+    [B,Hq,Sq] from the forward (same causal / seqlens_k / scale).  Returns (dq, dk, dv) bf16;
+    ``dsum`` (fp32 [B,Hq,Sq] scratch) is allocated when not given.
+    """
+    torch = _torch()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, S, H, D]")
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between q, k and v")
+    if tuple(out.shape) != tuple(q.shape) or tuple(dout.shape) != tuple(q.shape):
+        raise ValueError("out and dout must have q's shape")
+    if any(t.dtype != torch.bfloat16 for t in (q, k, v, out, dout)):
+        raise TypeError("gqa_bwd takes bf16 q, k, v, out, dout")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, Hq, Sq):
+        raise ValueError("lse must be float32 [B, Hq, Sq]")
+    if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or tuple(seqlens_k.shape) != (B,)):
+        raise ValueError("seqlens_k must be int32 [B]")
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    if dsum is None:
+        dsum = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    dev = _check_cuda(q, k, v, out, dout, lse, dsum, dq, dk, dv, seqlens_k)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    rc = load_library().gqa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dsum), _ptr(dq),
+                                _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)),
+                                _ptr(seqlens_k), GQA_DTYPE_BF16, _stream(dev, stream))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_bwd")
+    return dq, dk, dv
 
 
 def gqa_decode_num_splits(B, Hkv, max_seqlen_k, num_splits=0) -> int:

@@ -18,6 +18,7 @@
 #include "decode_sm103.cuh"
 #include "decode_fp8_sm103.cuh"
 #include "fp32_check.cuh"
+#include "backward_sm103.cuh"
 
 namespace {
 
@@ -236,6 +237,34 @@ bool decode_fp8_smem_attr_set(int dev) {
 }
 static_assert(gqa::decode::RingF8::kBytes >= sizeof(float) * (gqa::decode::kWarps * 8 * 128 + 2 * gqa::decode::kWarps * 8),
               "the fp8 decode merge reuses the ring memory");
+
+template <int D>
+bool bwd_smem_attr_set(int dev) {
+  static bool done[kMaxDevices] = {false};
+  if (dev >= 0 && dev < kMaxDevices && done[dev]) return true;
+  constexpr int bytes = int(gqa::bwd::Smem<D>::kBytes);
+  if (cudaFuncSetAttribute(gqa::bwd::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(gqa::bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+          cudaSuccess)
+    return false;
+  if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
+  return true;
+}
+
+// Dsum, then dQ and dK/dV (independent of each other) on one stream.
+template <int D>
+int launch_bwd(const gqa::bwd::Params& p, cudaStream_t stream) {
+  namespace bw = gqa::bwd;
+  if (!bwd_smem_attr_set<D>(current_device())) return GQA_ERR_CUDA;
+  const long long rows = (long long)p.B * p.Hq * p.Sq;
+  bw::dsum_kernel<D><<<unsigned((rows + 7) / 8), 256, 0, stream>>>(p);
+  const dim3 gq((p.Sq + bw::kT - 1) / bw::kT, p.Hq, p.B);
+  bw::dq_kernel<D><<<gq, bw::kThreads, bw::Smem<D>::kBytes, stream>>>(p);
+  const dim3 gk((p.Sk + bw::kT - 1) / bw::kT, p.Hkv, p.B);
+  bw::dkdv_kernel<D><<<gk, bw::kThreads, bw::Smem<D>::kBytes, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+}
 
 int launch_f32(const gqa::f32::Params& p, cudaStream_t stream) {
   const long long rows = p.cu_q ? (long long)p.Hq * p.total_q : (long long)p.B * p.Hq * p.Sq;
@@ -624,6 +653,47 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
     return GQA_OK;
   }
   return GQA_ERR_INVALID_ARG;
+}
+
+int gqa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+            float* dsum, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale,
+            int causal, const int* seqlens_k, int dtype, void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return GQA_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
+  if (!q || !k || !v || !out || !dout || !lse || !dsum || !dq || !dk || !dv) return GQA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
+  if (!aligned(lse, 4) || !aligned(dsum, 4) || (seqlens_k && !aligned(seqlens_k, 4))) return GQA_ERR_INVALID_ARG;
+  if (dtype != GQA_DTYPE_BF16) return dtype == GQA_DTYPE_FP32 ? GQA_ERR_UNSUPPORTED : GQA_ERR_INVALID_ARG;
+  for (const void* t : {q, k, v, out, dout, static_cast<const void*>(dq), static_cast<const void*>(dk),
+                        static_cast<const void*>(dv)})
+    if (!aligned(t, 16)) return GQA_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
+  if (Hq > 65535 || B > 65535 || (long long)Hq * D * Sq * B > (1LL << 40) ||
+      (long long)Hkv * D * Sk * B > (1LL << 40))
+    return GQA_ERR_UNSUPPORTED;
+  gqa::bwd::Params p{};
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.o = static_cast<const __nv_bfloat16*>(out);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.lse = lse;
+  p.seqlens = seqlens_k;
+  p.dsum = dsum;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.Sq = Sq;
+  p.Sk = Sk;
+  p.causal = causal;
+  p.scale = scale;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return D == 64 ? launch_bwd<64>(p, st) : launch_bwd<128>(p, st);
 }
 
 int gqa_device_status(void* stream) {

@@ -143,6 +143,15 @@ def make_prefill(B, Hq, Hkv, Sq, Sk, D, *, seed=0, lens=None, dtype="bf16", q_mu
     return dict(q=_cast(q, dtype), k=_cast(k, dtype), v=_cast(v, dtype), seqlens_k=seqlens)
 
 
+def make_backward(B, Hq, Hkv, Sq, Sk, D, *, seed=0, lens=None):
+    """make_prefill's bf16 inputs plus an upstream gradient dout [B,Sq,Hq,D] (standard normal,
+    drawn after them from the same generator)."""
+    d = make_prefill(B, Hq, Hkv, Sq, Sk, D, seed=seed, lens=lens, dtype="bf16")
+    g = torch.Generator("cpu").manual_seed(int(seed) + 7919)
+    d["dout"] = _cast(torch.randn((B, Sq, Hq, D), generator=g, dtype=torch.float32), "bf16")
+    return d
+
+
 def make_decode(B, Hq, Hkv, D, Smax, *, seed=0, lens=(1, None), dtype="bf16"):
     """Return dict(q [B,Hq,D], kcache, vcache [B,Smax,Hkv,D], cache_seqlens int32 [B])."""
     g = torch.Generator("cpu").manual_seed(int(seed))

@@ -157,6 +157,42 @@ int gqa_fwd_sparse(const void* q, const void* k, const void* v, void* out, float
                    int dtype, void* stream);
 
 /*
+ * gqa_bwd -- gradients of gqa_fwd (dense layout) with respect to q, k and v
+ * for an upstream gradient dout ([FA-SERIES] "V2" names a faster backward
+ * pass as one of its gains, and "Ana fikir" keeps the softmax intermediates
+ * out of slow memory; read here as: the weights are rebuilt from the
+ * forward's log-sum-exp, never stored.  [GQA-BERT] "GQA的分组共享机制": the
+ * G query heads of a group read one K/V head, so that head's gradient sums
+ * over the group).  With P_ij = exp(scale q_i.k_j - lse_i) over
+ * the admissible keys of gqa_fwd and Dsum_i = dout_i . out_i:
+ *     dv_j = sum_{h in group} sum_i P_ij dout_i
+ *     dS_ij = P_ij (dout_i . v_j - Dsum_i)
+ *     dq_i = scale sum_j dS_ij k_j
+ *     dk_j = scale sum_{h in group} sum_i dS_ij q_i
+ *
+ *   q, out, dout  [B, Sq, Hq, D] bf16 device (out: the forward's output)
+ *   k, v          [B, Sk, Hkv, D] bf16 device
+ *   lse           [B, Hq, Sq] fp32 device: the forward's log-sum-exp (rows
+ *                 with no admissible key hold -inf)
+ *   dsum          [B, Hq, Sq] fp32 device, caller-owned scratch; written
+ *                 with Dsum_i
+ *   dq            [B, Sq, Hq, D] bf16 device, written (every element)
+ *   dk, dv        [B, Sk, Hkv, D] bf16 device, written (every element;
+ *                 keys >= L_b get zeros)
+ *   scale, causal, seqlens_k  as gqa_fwd (and must be what it was given)
+ *   dtype         GQA_DTYPE_BF16 only (GQA_DTYPE_FP32 -> GQA_ERR_UNSUPPORTED)
+ * D 64 or 128 (GQA_ERR_UNSUPPORTED otherwise); all bf16 tensors 16-byte
+ * aligned; B, Hq <= 65535.  Gradients accumulate in fp32; P and dS are
+ * rounded to bf16 for the products.  No atomics: the result does not depend
+ * on scheduling.  Buffers must not overlap.  Launches three kernels on
+ * `stream` and returns without synchronising.
+ */
+int gqa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+            const float* lse, float* dsum, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
+            int Sq, int Sk, int D, float scale, int causal, const int* seqlens_k, int dtype,
+            void* stream);
+
+/*
  * gqa_decode_num_splits -- the number of KV-length splits gqa_decode will use.
  * num_splits in 1..128 is returned clamped to the number of 16-key blocks of
  * max_seqlen_k; num_splits <= 0 asks for the automatic choice, which sizes

@@ -169,3 +169,23 @@ def test_fwd_sparse_rejects_invalid_arguments(lib, kw):
 def test_fwd_sparse_unsupported_shapes(lib):
     assert _sparse(lib, Sk=8193) == gqa.GQA_ERR_UNSUPPORTED      # more than 64 key tiles of 128
     assert _sparse(lib, D=96) == gqa.GQA_ERR_UNSUPPORTED
+
+
+def _bwd(lib, B=1, Hq=4, Hkv=2, Sq=8, Sk=8, D=64, scale=0.125, causal=0, dtype=0, q=FAKE, lse=FAKE, dsum=FAKE,
+         dk=FAKE):
+    P = ctypes.c_void_p
+    return lib.gqa_bwd(P(q), P(FAKE), P(FAKE), P(FAKE), P(FAKE), P(lse) if lse else None, P(dsum) if dsum else None,
+                       P(FAKE), P(dk), P(FAKE), B, Hq, Hkv, Sq, Sk, D, scale, causal, None, dtype, None)
+
+
+@pytest.mark.parametrize("kw", [dict(lse=0), dict(dsum=0), dict(Hq=6, Hkv=4), dict(B=0), dict(Sk=0),
+                                dict(scale=float("inf")), dict(causal=2), dict(q=FAKE + 8), dict(dk=FAKE + 2),
+                                dict(lse=FAKE + 2), dict(dtype=7)])
+def test_bwd_rejects_invalid_arguments(lib, kw):
+    assert _bwd(lib, **kw) == gqa.GQA_ERR_INVALID_ARG
+
+
+def test_bwd_unsupported(lib):
+    assert _bwd(lib, dtype=gqa.GQA_DTYPE_FP32) == gqa.GQA_ERR_UNSUPPORTED   # bf16 only
+    assert _bwd(lib, D=96) == gqa.GQA_ERR_UNSUPPORTED
+    assert _bwd(lib, B=70000) == gqa.GQA_ERR_UNSUPPORTED                   # grid z limit

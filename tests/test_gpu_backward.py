@@ -1,0 +1,121 @@
+"""GPU parity of gqa_bwd (dQ, dK, dV of grouped-query attention) against the
+fp64 oracle, through the C ABI.
+
+The kernel is given the forward's output and log-sum-exp.  The main cases
+take both from the oracle's forward (rounded to bf16 / fp32 as the API
+stores them), so that only the backward kernels are under test; one case
+chains the library's own forward.
+
+Tolerance (bf16 inputs and outputs, fp32 accumulation, P and dS rounded to
+bf16 before the products, Dsum formed from the bf16 forward output): each
+gradient rounds to bf16 on output (relative 2^-9), and the per-product
+roundings add errors of the same relative size that partly cancel over the
+sums.  The test asks for relative L2 error <= 1e-2 and max-abs error <=
+2e-2 * max |ref| + 1e-4 for every gradient tensor.  The absolute floor
+covers gradients that vanish exactly: with one admissible key P = 1 and
+dS = dO.v - dO.O = 0 in exact arithmetic, but the kernel's Dsum uses the
+bf16-rounded O, leaving |dS| ~ 2^-9 |dO| |O|, i.e. dq ~ 1e-7 here.
+"""
+import numpy as np
+import pytest
+import torch
+
+import grouped_query_attention_08_b300 as gqa
+import oracle
+from grouped_query_attention_08_b300 import build, inputs
+
+pytestmark = pytest.mark.gpu
+
+REL_L2, MAX_REL, ABS_FLOOR = 1e-2, 2e-2, 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    gqa.load_library()
+
+
+def _cmp(got, ref, what):
+    got = got.float().cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got)), "%s has non-finite values" % what
+    err = np.abs(got - ref)
+    scale = max(float(np.abs(ref).max()), 1e-30)
+    rel = float(np.linalg.norm(got - ref) / max(np.linalg.norm(ref), 1e-30))
+    msg = "%s: rel-l2 %.3g, max-abs %.3g of max|ref| %.3g" % (what, rel, float(err.max()), scale)
+    assert float(err.max()) <= MAX_REL * scale + ABS_FLOOR, msg
+    if np.linalg.norm(ref) > 1e3 * ABS_FLOOR:
+        assert rel <= REL_L2, msg
+
+
+def _oracle_fwd(inp, scale, causal):
+    out, lse = oracle.attention(inp["q"], inp["k"], inp["v"], scale=scale, causal=causal,
+                                seqlens_k=inp.get("seqlens_k"))
+    return (torch.from_numpy(np.ascontiguousarray(out)).to(torch.bfloat16),
+            torch.from_numpy(np.ascontiguousarray(lse)).to(torch.float32))
+
+
+def _run(inp, out, lse, scale, causal):
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    dq, dk, dv = gqa.gqa_bwd(d["q"], d["k"], d["v"], out.cuda(), d["dout"], lse.cuda(), causal=causal,
+                             seqlens_k=d["seqlens_k"], scale=scale)
+    torch.cuda.synchronize()
+    assert gqa.gqa_device_status() == 0
+    return dq, dk, dv
+
+
+# (B, Hq, Hkv, Sq, Sk, D, causal, lens)
+CASES = [
+    (2, 8, 2, 200, 300, 64, False, (1, 300)),    # G=4, ragged tiles, padded keys
+    (1, 12, 3, 256, 256, 64, True, None),        # BERT-style grouping, causal
+    (2, 8, 8, 130, 190, 128, False, None),       # MHA, D=128, ragged
+    (1, 16, 2, 100, 400, 128, True, None),       # G=8, causal with Sq < Sk
+    (1, 4, 1, 300, 120, 64, True, None),         # MQA, causal with Sq > Sk: rows with no key
+    (2, 4, 2, 70, 70, 64, False, (0, 70)),       # an empty key set possible
+    (1, 2, 1, 1, 1, 128, False, None),           # one query, one key
+]
+
+
+def _ids(c):
+    return "B%dHq%dHkv%dSq%dSk%dD%d%s%s" % (c[0], c[1], c[2], c[3], c[4], c[5], "c" if c[6] else "n",
+                                           "_lens" if c[7] else "")
+
+
+@pytest.mark.parametrize("case", CASES, ids=_ids)
+def test_bwd_matches_oracle(case):
+    B, Hq, Hkv, Sq, Sk, D, causal, lens = case
+    inp = inputs.make_backward(B, Hq, Hkv, Sq, Sk, D, seed=Sq * 3 + Sk + D, lens=lens)
+    scale = 1.0 / np.sqrt(D)
+    out, lse = _oracle_fwd(inp, scale, causal)
+    rq, rk, rv = oracle.attention_backward(inp["q"], inp["k"], inp["v"], inp["dout"], scale=scale, causal=causal,
+                                           seqlens_k=inp["seqlens_k"])
+    dq, dk, dv = _run(inp, out, lse, scale, causal)
+    _cmp(dq, rq, "dq")
+    _cmp(dk, rk, "dk")
+    _cmp(dv, rv, "dv")
+
+
+def test_bwd_after_library_forward():
+    inp = inputs.make_backward(2, 12, 3, 333, 333, 64, seed=11, lens=(200, 333))
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out, lse = gqa.gqa_fwd(d["q"], d["k"], d["v"], causal=True, seqlens_k=d["seqlens_k"], scale=0.125)
+    dq, dk, dv = gqa.gqa_bwd(d["q"], d["k"], d["v"], out, d["dout"], lse, causal=True, seqlens_k=d["seqlens_k"],
+                             scale=0.125)
+    torch.cuda.synchronize()
+    assert gqa.gqa_device_status() == 0
+    rq, rk, rv = oracle.attention_backward(inp["q"], inp["k"], inp["v"], inp["dout"], scale=0.125, causal=True,
+                                           seqlens_k=inp["seqlens_k"])
+    _cmp(dq, rq, "dq")
+    _cmp(dk, rk, "dk")
+    _cmp(dv, rv, "dv")
+
+
+def test_bwd_is_deterministic_and_zero_past_the_key_length():
+    inp = inputs.make_backward(2, 8, 2, 150, 260, 128, seed=5, lens=(40, 200))
+    out, lse = _oracle_fwd(inp, 0.09, False)
+    a = _run(inp, out, lse, 0.09, False)
+    b = _run(inp, out, lse, 0.09, False)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    lens = inp["seqlens_k"].tolist()
+    for bi, L in enumerate(lens):
+        assert torch.all(a[1][bi, L:] == 0) and torch.all(a[2][bi, L:] == 0)
