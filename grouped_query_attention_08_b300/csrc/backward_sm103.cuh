@@ -1,65 +1,73 @@
-// backward_sm103.cuh -- gradients of the GQA forward (dQ, dK, dV), bf16.
+// backward_sm103.cuh -- gradients of the GQA forward (dQ, dK, dV), bf16, on
+// the tcgen05 tensor cores with TMEM accumulators.
 //
 // Sources (page title and section): "FlashAttention Serisi"
 // (webturing.pages.dev), "V2" (a faster backward pass is one of its gains)
 // and "Ana fikir" (the softmax intermediates stay out of slow memory; read
 // here as: the weights are rebuilt from the forward's log-sum-exp, nothing
-// quadratic is stored); "3个GQA核心优化技巧"
-// (blog.gitcode.com), "GQA的分组共享机制": the G query heads of a group
-// share one K/V head, so that head's gradient is the sum over the group.
+// quadratic is stored); "3个GQA核心优化技巧" (blog.gitcode.com),
+// "GQA的分组共享机制": the G query heads of a group share one K/V head, so
+// that head's gradient is the sum over the group.
 //
 // With P_ij = exp(scale q_i.k_j - lse_i) over the admissible keys (lse from
 // the forward), Dsum_i = dO_i . O_i:
 //   dV_j = sum_{h in group, i} P_ij dO_i
 //   dS_ij = P_ij (dO_i . v_j - Dsum_i)
 //   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_{h in group, i} dS_ij q_i
-// Three kernels, no atomics: Dsum per query row; dQ per (b, h, 64 queries)
-// looping over key tiles; dK and dV per (b, kvh, 64 keys) looping over the
-// group's heads and the query tiles.  Tiles are staged in shared memory and
-// multiplied with WMMA (16x16x16 bf16, fp32 accumulate); P and dS are
-// rounded to bf16 for the products.
+// Three kernels, no atomics, so the result does not depend on scheduling:
+//  * dsum_kernel: Dsum per query row.
+//  * dq_kernel, one CTA per (b, kvh, Mq tokens x G heads = one 128-row tile,
+//    row = token * G + head-in-group, as in the forward): per 128-key tile
+//    S = Q K^T and dP = dO V^T into TMEM, dS = P (dP - Dsum) written back
+//    over S as packed bf16, dQ += dS K accumulated in TMEM.
+//  * dkdv_kernel, one CTA per (b, kvh, 128 keys): for every head of the group
+//    and every query tile of 128, S^T = K Q^T and dP^T = V dO^T into TMEM,
+//    P^T and dS^T written back over them, dV += P^T dO and dK += dS^T Q
+//    accumulated in TMEM over the whole loop (the group sum).
+// Warp roles (192 threads): warps 0-3 one TMEM lane (tile row) per thread for
+// the elementwise step and the epilogue, warp 4 TMA producer, warp 5 MMA
+// issuer.  Tiles arrive by TMA with the 128-byte swizzle; operands that stay
+// fixed for the whole CTA (Q and dO in dq_kernel, K and V in dkdv_kernel at
+// D = 64) are copied into TMEM with tcgen05.cp and read from there as the A
+// operand, which leaves the shared-memory operand bandwidth to the streamed
+// tiles.  All waits are bounded: on a timeout the kernel raises a device
+// error, drains its copies and MMAs, and exits.
 #pragma once
-
-#include <mma.h>
 
 #include "common.cuh"
 
 namespace gqa {
 namespace bwd {
 
-namespace wm = nvcuda::wmma;
-
-constexpr int kT = 64;          // queries per dQ CTA, keys per dK/dV CTA, tile edge
-constexpr int kWarps = 4;       // 16 rows each
-constexpr int kThreads = kWarps * 32;
+constexpr int kThreads = 192;
+constexpr int kWarpTMA = 4;
+constexpr int kWarpMMA = 5;
+constexpr int kBN = 128;                 // keys per tile (dq_kernel); keys per CTA (dkdv_kernel)
+constexpr int kBQ = 128;                 // queries per tile (dkdv_kernel)
+constexpr uint32_t kHalfBytes = 128u * 128u;   // 128 rows x 64 bf16 (128 bytes), one swizzle span
+constexpr float kLog2e = 1.4426950408889634f;
 
 struct Params {
-  const __nv_bfloat16* q;       // [B, Sq, Hq, D]
-  const __nv_bfloat16* k;       // [B, Sk, Hkv, D]
-  const __nv_bfloat16* v;       // [B, Sk, Hkv, D]
-  const __nv_bfloat16* o;       // [B, Sq, Hq, D]  forward output
-  const __nv_bfloat16* dout;    // [B, Sq, Hq, D]
+  const __nv_bfloat16* o;       // [B, Sq, Hq, D]  forward output (dsum_kernel)
+  const __nv_bfloat16* dout;    // [B, Sq, Hq, D]  (dsum_kernel)
   const float* lse;             // [B, Hq, Sq]     forward log-sum-exp (natural log)
   const int* seqlens;           // [B] or nullptr
-  float* dsum;                  // [B, Hq, Sq]     workspace
+  float* dsum;                  // [B, Hq, Sq]     Dsum, written by dsum_kernel
   __nv_bfloat16* dq;            // [B, Sq, Hq, D]
   __nv_bfloat16* dk;            // [B, Sk, Hkv, D]
   __nv_bfloat16* dv;            // [B, Sk, Hkv, D]
-  int B, Hq, Hkv, G, Sq, Sk, causal;
+  int B, Hq, Hkv, G, Sq, Sk;
+  int Mq;                       // tokens per dq_kernel tile (G * Mq <= 128)
+  int n_qt;                     // dq_kernel tiles per (b, kvh): ceil(Sq / Mq)
+  int n_kt;                     // dkdv_kernel tiles per (b, kvh): ceil(Sk / 128)
+  int causal;
   float scale;
+  float scale_log2;             // scale * log2(e)
+  unsigned long long timeout_ns;
 };
 
-template <int D>
-struct Smem {
-  static constexpr int kLd = D + 8;          // bf16 tile row (elements); 16-row steps stay 32-byte aligned
-  static constexpr int kLdS = kT + 4;        // fp32 score tile row (elements)
-  static constexpr int kTile = kT * kLd;     // elements of a 64 x D bf16 tile
-  // a: Q (dQ) or K (dK/dV); b: dO or V; c: K or Q; d: V or dO (bf16 tiles);
-  // per warp a 16 x 64 fp32 S tile, a 16 x 64 fp32 dP tile, two 16 x 64 bf16 tiles
-  static constexpr size_t kBytes = 4 * size_t(kTile) * 2 + kWarps * (2 * 16 * kLdS * 4 + 2 * 16 * (kT + 8) * 2) +
-                                   2 * kT * 4;
-};
-
+// Key length of batch entry b (a bad length raises a device error and
+// counts as zero).
 DEVI int key_len(const Params& p, int b) {
   int L = p.seqlens ? p.seqlens[b] : p.Sk;
   if (L < 0 || L > p.Sk) {
@@ -67,19 +75,6 @@ DEVI int key_len(const Params& p, int b) {
     L = 0;
   }
   return L;
-}
-
-// Rows [r0, r0 + 64) of the [S, H, D] slice `head` of batch b into a
-// padded shared-memory tile; rows >= S are zero.  16-byte loads.
-template <int D>
-DEVI void load_tile(__nv_bfloat16* dst, const __nv_bfloat16* src, int b, int S, int H, int head, int r0) {
-  constexpr int kChunks = D / 8;
-  for (int e = threadIdx.x; e < kT * kChunks; e += kThreads) {
-    const int r = e / kChunks, c = e % kChunks;
-    uint4 w = make_uint4(0u, 0u, 0u, 0u);
-    if (r0 + r < S) w = *reinterpret_cast<const uint4*>(src + ((size_t(b) * S + r0 + r) * H + head) * D + 8 * c);
-    *reinterpret_cast<uint4*>(dst + r * Smem<D>::kLd + 8 * c) = w;
-  }
 }
 
 // Dsum_i = dO_i . O_i, one warp per (b, h, i).
@@ -100,196 +95,584 @@ __global__ void __launch_bounds__(256) dsum_kernel(const Params p) {
   if (lane == 0) p.dsum[row] = acc;
 }
 
-// Shared-memory carve-up: four bf16 64 x D tiles, then per warp an fp32
-// S tile, an fp32 dP tile and two bf16 16 x 64 tiles, then two fp32 row
-// vectors of 64 (lse and Dsum of the tile's query rows).
+// Shared-memory operand descriptors of a swizzled 128-row tile stored as
+// 64-column halves of kHalfBytes each.
+// K-major (the contraction runs along the tile's columns): 16-column step ks.
+DEVI uint64_t desc_kmajor(uint32_t tile, int ks) {
+  return make_sdesc_sw128(tile + uint32_t(ks / 4) * kHalfBytes + uint32_t(ks % 4) * 32u, 16, 1024);
+}
+// MN-major B (the contraction runs along the tile's rows, N along its
+// columns): 16-row step ks; 8-row groups are 1024 bytes apart, and the second
+// 64-column half (D = 128) is kHalfBytes further.
 template <int D>
-struct Carve {
-  __nv_bfloat16* t[4];
-  float* s;
-  float* dp;
-  __nv_bfloat16* x;
-  __nv_bfloat16* y;
-  float* lse;
-  float* dsum;
-  DEVI Carve(uint8_t* base, int warp) {
-    using SM = Smem<D>;
-    __nv_bfloat16* tb = reinterpret_cast<__nv_bfloat16*>(base);
-    for (int i = 0; i < 4; ++i) t[i] = tb + i * SM::kTile;
-    uint8_t* w = base + 4 * size_t(SM::kTile) * 2 +
-                 size_t(warp) * (2 * 16 * SM::kLdS * 4 + 2 * 16 * (kT + 8) * 2);
-    s = reinterpret_cast<float*>(w);
-    dp = s + 16 * SM::kLdS;
-    x = reinterpret_cast<__nv_bfloat16*>(dp + 16 * SM::kLdS);
-    y = x + 16 * (kT + 8);
-    float* rv = reinterpret_cast<float*>(base + 4 * size_t(SM::kTile) * 2 +
-                                         kWarps * (2 * 16 * SM::kLdS * 4 + 2 * 16 * (kT + 8) * 2));
-    lse = rv;
-    dsum = rv + kT;
+DEVI uint64_t desc_mnmajor(uint32_t tile, int ks) {
+  return make_sdesc_sw128(tile + uint32_t(ks) * 2048u, D == 64 ? 1024u : kHalfBytes, 1024);
+}
+// Copies a K-major 128-row tile of D columns into TMEM columns
+// [col, col + D/2) as packed bf16 pairs, the layout of a TMEM A operand.
+template <int D>
+DEVI void copy_tile_to_tmem(uint32_t tcol, uint32_t tile) {
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) tmem_cp_128x256b(tcol + uint32_t(ks) * 8u, desc_kmajor(tile, ks));
+}
+
+// Writes 32 fp32 values times `mul` as bf16 to dst (16-byte aligned).
+DEVI void store_row32(__nv_bfloat16* dst, const uint32_t* v, float mul) {
+#pragma unroll
+  for (int c8 = 0; c8 < 4; ++c8) {
+    uint4 w;
+    w.x = pack_bf16x2(__uint_as_float(v[8 * c8 + 0]) * mul, __uint_as_float(v[8 * c8 + 1]) * mul);
+    w.y = pack_bf16x2(__uint_as_float(v[8 * c8 + 2]) * mul, __uint_as_float(v[8 * c8 + 3]) * mul);
+    w.z = pack_bf16x2(__uint_as_float(v[8 * c8 + 4]) * mul, __uint_as_float(v[8 * c8 + 5]) * mul);
+    w.w = pack_bf16x2(__uint_as_float(v[8 * c8 + 6]) * mul, __uint_as_float(v[8 * c8 + 7]) * mul);
+    *reinterpret_cast<uint4*>(dst + 8 * c8) = w;
   }
+}
+DEVI void store_zero_row(__nv_bfloat16* dst, int n) {
+  for (int c = 0; c < n; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// ------------------------------------------------------------------ dq_kernel
+template <int D>
+struct DqLayout {
+  static constexpr int kHalves = D / 64;
+  static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kStages = (D == 64) ? 3 : 2;        // K/V ring depth
+  static constexpr uint32_t kOffQ = 0;
+  static constexpr uint32_t kOffDO = kTileBytes;
+  static constexpr uint32_t kOffK = 2 * kTileBytes;
+  static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
+  static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
+  // q_full, kv_full[S], kv_empty[S], s_full, p_full, done, drain
+  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  static constexpr uint32_t kOffSlot = kOffBar + 8u * kNumBars;
+  static constexpr uint32_t kOffAbort = kOffSlot + 8u;
+  static constexpr uint32_t kBytes = kOffAbort + 8u;
+  static constexpr uint32_t kSmemAlloc = kBytes + 1024u;
+  // TMEM: S [0,128) (dS over its first 64 as bf16 pairs), dP [128,256),
+  // Q [256, 256+D/2), dO [256+D/2, 256+D), dQ [256+D, 256+2D)
+  static constexpr uint32_t kTmS = 0, kTmP = 128, kTmQ = 256, kTmDO = 256 + D / 2, kTmDQ = 256 + D;
+  static constexpr uint32_t kTmCols = 512;
+  static_assert(kTmDQ + D <= kTmCols, "TMEM column map overflows");
+  static_assert(kSmemAlloc > 116u * 1024u, "one CTA per SM: its TMEM allocation takes all 512 columns");
 };
 
-// C (16 x 64, fp32, row stride ldc) = A (16 x D rows of a, row-major) .
-// B^T where B is 64 x D rows of b (so B^T is b read column-major).
+// ---------------------------------------------------------------- dkdv_kernel
 template <int D>
-DEVI void mm_abt(float* c, int ldc, const __nv_bfloat16* a, const __nv_bfloat16* b) {
-  constexpr int ld = Smem<D>::kLd;
-#pragma unroll
-  for (int n = 0; n < kT / 16; ++n) {
-    wm::fragment<wm::accumulator, 16, 16, 16, float> acc;
-    wm::fill_fragment(acc, 0.f);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      wm::fragment<wm::matrix_a, 16, 16, 16, __nv_bfloat16, wm::row_major> fa;
-      wm::fragment<wm::matrix_b, 16, 16, 16, __nv_bfloat16, wm::col_major> fb;
-      wm::load_matrix_sync(fa, a + kk * 16, ld);
-      wm::load_matrix_sync(fb, b + n * 16 * ld + kk * 16, ld);
-      wm::mma_sync(acc, fa, fb, acc);
-    }
-    wm::store_matrix_sync(c + n * 16, acc, ldc, wm::mem_row_major);
-  }
-}
+struct KvLayout {
+  static constexpr int kHalves = D / 64;
+  static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kStages = (D == 64) ? 3 : 2;        // Q/dO ring depth
+  static constexpr bool kKVInTmem = (D == 64);             // K, V copied into TMEM as A operands
+  static constexpr uint32_t kOffK = 0;
+  static constexpr uint32_t kOffV = kTileBytes;
+  static constexpr uint32_t kOffQ = 2 * kTileBytes;
+  static constexpr uint32_t kOffDO = kOffQ + kStages * kTileBytes;
+  static constexpr uint32_t kOffRow = kOffDO + kStages * kTileBytes;   // [2][2][128] fp32: lse*log2e, Dsum
+  static constexpr uint32_t kOffBar = kOffRow + 2u * 2u * kBQ * 4u;
+  // kv_full, qd_full[S], qd_empty[S], s_full, p_full, done, drain, row_full[2]
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2;
+  static constexpr uint32_t kOffSlot = kOffBar + 8u * kNumBars;
+  static constexpr uint32_t kOffAbort = kOffSlot + 8u;
+  static constexpr uint32_t kBytes = kOffAbort + 8u;
+  static constexpr uint32_t kSmemAlloc = kBytes + 1024u;
+  // TMEM: S^T [0,128) (P^T over its first 64), dP^T [128,256) (dS^T over its
+  // first 64), dV [256, 256+D), dK [256+D, 256+2D), and at D = 64 K, V.
+  static constexpr uint32_t kTmS = 0, kTmP = 128, kTmDV = 256, kTmDK = 256 + D;
+  static constexpr uint32_t kTmK = 256 + 2 * D, kTmV = 256 + 2 * D + D / 2;
+  static constexpr uint32_t kTmCols = 512;
+  static_assert(!kKVInTmem || kTmV + D / 2 <= kTmCols, "TMEM column map overflows");
+  static_assert(kKVInTmem || kTmDK + D <= kTmCols, "TMEM column map overflows");
+  static_assert(kSmemAlloc > 116u * 1024u, "one CTA per SM: its TMEM allocation takes all 512 columns");
+};
 
-// acc[n] (16 x 16 blocks of a 16 x D result) += X (16 x 64 bf16, row stride
-// kT + 8) . T (64 x D rows of a shared tile, row-major).
+// dQ for one 128-row tile (Mq tokens x G heads of K/V head kvh, batch b).
+// Per key tile j the issuer runs S(j) = Q K(j)^T and dP(j) = dO V(j)^T, the
+// elementwise warps turn them into dS(j) (bf16 over S), then the issuer runs
+// dQ += dS(j) K(j) followed by S(j+1), dP(j+1) (in issue order, so S(j+1)
+// overwrites dS(j) only after it has been read).
 template <int D>
-DEVI void mm_acc(wm::fragment<wm::accumulator, 16, 16, 16, float> (&acc)[D / 16], const __nv_bfloat16* x,
-                 const __nv_bfloat16* t) {
-  constexpr int ld = Smem<D>::kLd;
-#pragma unroll
-  for (int kk = 0; kk < kT / 16; ++kk) {
-    wm::fragment<wm::matrix_a, 16, 16, 16, __nv_bfloat16, wm::row_major> fa;
-    wm::load_matrix_sync(fa, x + kk * 16, kT + 8);
-#pragma unroll
-    for (int n = 0; n < D / 16; ++n) {
-      wm::fragment<wm::matrix_b, 16, 16, 16, __nv_bfloat16, wm::row_major> fb;
-      wm::load_matrix_sync(fb, t + kk * 16 * ld + n * 16, ld);
-      wm::mma_sync(acc[n], fa, fb, acc[n]);
-    }
-  }
-}
-
-// Writes scale * acc (16 x D) as bf16 rows row0.. (rows >= S skipped) of the
-// [S, H, D] slice `head` of batch b, through the warp's fp32 S tile.
-template <int D>
-DEVI void store_rows(wm::fragment<wm::accumulator, 16, 16, 16, float> (&acc)[D / 16], float* stage, float scale,
-                     __nv_bfloat16* dst, int b, int S, int H, int head, int row0) {
-  constexpr int ldc = Smem<D>::kLdS;      // the 16 x 64 stage holds 64 columns at a time
+__global__ void __launch_bounds__(kThreads, 1)
+    dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+              const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using L = DqLayout<D>;
+  constexpr int S = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw_addr);
+  const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-#pragma unroll
-  for (int half = 0; half < D / 64; ++half) {
-#pragma unroll
-    for (int n = 0; n < 4; ++n) wm::store_matrix_sync(stage + n * 16, acc[4 * half + n], ldc, wm::mem_row_major);
-    __syncwarp();
-    for (int e = lane; e < 16 * 64; e += 32) {
-      const int r = e >> 6, c = e & 63;
-      if (row0 + r < S)
-        dst[((size_t(b) * S + row0 + r) * H + head) * D + 64 * half + c] = __float2bfloat16_rn(stage[r * ldc + c] * scale);
+  auto bar = [&](int i) -> uint32_t { return base + L::kOffBar + 8u * uint32_t(i); };
+  const uint32_t q_full = bar(0);
+  auto kv_full = [&](int s) { return bar(1 + s); };
+  auto kv_empty = [&](int s) { return bar(1 + S + s); };
+  const uint32_t s_full = bar(1 + 2 * S), p_full = bar(2 + 2 * S), done = bar(3 + 2 * S), drain = bar(4 + 2 * S);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffSlot);
+  const uint64_t to = p.timeout_ns;
+
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int q0 = blockIdx.x * p.Mq;
+  const int Lb = key_len(p, b);
+  const int diag = p.Sk - p.Sq;               // causal: query i sees keys j <= i + diag
+  int kmax = Lb;
+  if (p.causal) kmax = min(kmax, min(q0 + p.Mq, p.Sq) - 1 + diag + 1);
+  const int n = kmax > 0 ? (kmax + kBN - 1) / kBN : 0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(kv_full(s), 1);
+      mbar_init(kv_empty(s), 1);
     }
-    __syncwarp();
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 4);        // one arrival per elementwise warp
+    mbar_init(done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
+  }
+  if (warp == kWarpMMA) {
+    tmem_alloc(smem_u32(tmem_slot), L::kTmCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpTMA && lane == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmDO);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kWarpTMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      const uint32_t q_bytes = 2u * uint32_t(L::kHalves) * 128u * uint32_t(p.G * p.Mq);
+      mbar_arrive_expect_tx(q_full, q_bytes);
+      for (int hh = 0; hh < L::kHalves; ++hh) {
+        tma_load_4d(base + L::kOffQ + hh * kHalfBytes, &tmQ, q_full, hh * 64, kvh * p.G, q0, b);
+        tma_load_4d(base + L::kOffDO + hh * kHalfBytes, &tmDO, q_full, hh * 64, kvh * p.G, q0, b);
+      }
+      bool ok = true;
+      int j = 0;
+      for (; j < n; ++j) {
+        const int s = j % S;
+        ok = mbar_wait(kv_empty(s), ((j / S) & 1) ^ 1, abort_flag, to);
+        if (!ok) break;
+        mbar_arrive_expect_tx(kv_full(s), 2u * L::kTileBytes);
+        for (int hh = 0; hh < L::kHalves; ++hh) {
+          tma_load_4d(base + L::kOffK + s * L::kTileBytes + hh * kHalfBytes, &tmK, kv_full(s), hh * 64, kvh,
+                      j * kBN, b);
+          tma_load_4d(base + L::kOffV + s * L::kTileBytes + hh * kHalfBytes, &tmV, kv_full(s), hh * 64, kvh,
+                      j * kBN, b);
+        }
+      }
+      if (!ok) {
+        // let the copies in flight land before the CTA exits: each waited
+        // phase belongs to the last load issued into its buffer
+        volatile int no_abort = 0;
+        for (int it = j > S ? j - S : 0; it < j; ++it)
+          mbar_wait(kv_full(it % S), (it / S) & 1, &no_abort, 200000000ull);
+        mbar_wait(q_full, 0, &no_abort, 200000000ull);
+      }
+    }
+  } else if (warp == kWarpMMA) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && n > 0) {
+      const uint32_t idesc_s = make_idesc_bf16(128, kBN, 0, 0);   // A in TMEM, B K-major
+      const uint32_t idesc_q = make_idesc_bf16(128, D, 0, 1);     // dS in TMEM, K MN-major
+      bool ok = mbar_wait(q_full, 0, abort_flag, to);
+      if (ok) {
+        tc_fence_after();
+        copy_tile_to_tmem<D>(tmem + L::kTmQ, base + L::kOffQ);
+        copy_tile_to_tmem<D>(tmem + L::kTmDO, base + L::kOffDO);
+      }
+      for (int j = 0; ok && j <= n; ++j) {
+        if (j < n) ok = mbar_wait(kv_full(j % S), (j / S) & 1, abort_flag, to);
+        if (ok && j > 0) ok = mbar_wait(p_full, (j - 1) & 1, abort_flag, to);
+        if (!ok) break;
+        tc_fence_after();
+        if (j > 0) {
+          // dQ += dS(j-1) K(j-1)
+          const int sp = (j - 1) % S;
+          const uint32_t ka = base + L::kOffK + sp * L::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks)
+            umma_ts(tmem + L::kTmDQ, tmem + L::kTmS + uint32_t(ks) * 8u, desc_mnmajor<D>(ka, ks), idesc_q,
+                    (j > 1 || ks > 0) ? 1u : 0u);
+          umma_commit(kv_empty(sp));
+          if (j == n) umma_commit(done);
+        }
+        if (j < n) {
+          const int s = j % S;
+          const uint32_t ka = base + L::kOffK + s * L::kTileBytes;
+          const uint32_t va = base + L::kOffV + s * L::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            umma_ts(tmem + L::kTmS, tmem + L::kTmQ + uint32_t(ks) * 8u, desc_kmajor(ka, ks), idesc_s,
+                    ks > 0 ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks)
+            umma_ts(tmem + L::kTmP, tmem + L::kTmDO + uint32_t(ks) * 8u, desc_kmajor(va, ks), idesc_s,
+                    ks > 0 ? 1u : 0u);
+          umma_commit(s_full);
+        }
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        umma_commit(drain);
+        mbar_wait(drain, 0, &no_abort, 200000000ull);
+      }
+    }
+  } else {
+    // ------------------------------------------------- elementwise + epilogue
+    const int r = warp * 32 + lane;                     // tile row = TMEM lane
+    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    const int token = r / p.G, gg = r - token * p.G;
+    const int i = q0 + token;
+    const bool row_ok = r < p.G * p.Mq && i < p.Sq;
+    const int h = kvh * p.G + gg;
+    const size_t rowidx = (size_t(b) * p.Hq + h) * p.Sq + i;
+    float lse2 = 0.f, dsum = 0.f;
+    int hi_row = 0;                                     // the row admits keys j < hi_row
+    if (row_ok) {
+      lse2 = p.lse[rowidx] * kLog2e;
+      dsum = p.dsum[rowidx];
+      hi_row = p.causal ? min(Lb, i + diag + 1) : Lb;
+    }
+    const float cl = p.scale_log2;
+    bool aborted = false;
+    for (int j = 0; j < n; ++j) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, to));
+      if (!ok) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      const int lim = hi_row - j * kBN;
+      const bool full = __all_sync(0xffffffffu, lim >= kBN || !row_ok);
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t sv[32], dp[32], ds[16];
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(c) * 32u, sv);
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(c) * 32u, dp);
+        tmem_ld_wait_x32(sv);
+        tmem_ld_wait_x32(dp);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int k0 = c * 32 + 2 * e;
+          const bool ok0 = full ? row_ok : (k0 < lim);
+          const bool ok1 = full ? row_ok : (k0 + 1 < lim);
+          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), cl, -lse2));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), cl, -lse2));
+          const float d0 = ok0 ? p0 * (__uint_as_float(dp[2 * e]) - dsum) : 0.f;
+          const float d1 = ok1 ? p1 * (__uint_as_float(dp[2 * e + 1]) - dsum) : 0.f;
+          ds[e] = pack_bf16x2(d0, d1);
+        }
+        tmem_st_32x32b_x16(tmem + lane_base + L::kTmS + uint32_t(c) * 16u, ds);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    __nv_bfloat16* drow = p.dq + ((size_t(b) * p.Sq + i) * p.Hq + h) * D;
+    if (n > 0 && !aborted) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, to));
+      tc_fence_after();
+      if (ok) {
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDQ + uint32_t(c), v);
+          tmem_ld_wait_x32(v);
+          if (row_ok) store_row32(drow + c, v, p.scale);
+        }
+      }
+    } else if (n == 0 && row_ok) {
+      store_zero_row(drow, D);               // no admissible key: dQ = 0
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmCols);
   }
 }
 
+// dK and dV for 128 keys of K/V head kvh, batch b.  Iteration it covers head
+// kvh * G + it / nqe of the group and query tile qfirst + it % nqe: the
+// issuer runs S^T = K Q^T and dP^T = V dO^T, the elementwise warps write
+// P^T and dS^T (bf16) over them, then the issuer runs dV += P^T dO and
+// dK += dS^T Q followed by the next iteration's S^T and dP^T.
 template <int D>
-__global__ void __launch_bounds__(kThreads) dq_kernel(const Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  Carve<D> cv(smem, warp);
-  __nv_bfloat16 *sQ = cv.t[0], *sdO = cv.t[1], *sK = cv.t[2], *sV = cv.t[3];
-  const int q0 = blockIdx.x * kT, h = blockIdx.y, b = blockIdx.z, kvh = h / p.G;
+__global__ void __launch_bounds__(kThreads, 1)
+    dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO, const Params p) {
+  using L = KvLayout<D>;
+  constexpr int S = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* sbase = smem_raw + (base - raw_addr);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  auto bar = [&](int i) -> uint32_t { return base + L::kOffBar + 8u * uint32_t(i); };
+  const uint32_t kv_full = bar(0);
+  auto qd_full = [&](int s) { return bar(1 + s); };
+  auto qd_empty = [&](int s) { return bar(1 + S + s); };
+  const uint32_t s_full = bar(1 + 2 * S), p_full = bar(2 + 2 * S), done = bar(3 + 2 * S), drain = bar(4 + 2 * S);
+  auto row_full = [&](int i) { return bar(5 + 2 * S + i); };
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffSlot);
+  float* rowv = reinterpret_cast<float*>(sbase + L::kOffRow);   // [2][2][kBQ]: lse * log2(e), Dsum
+  const uint64_t to = p.timeout_ns;
+
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int k0 = blockIdx.x * kBN;
   const int Lb = key_len(p, b);
-  load_tile<D>(sQ, p.q, b, p.Sq, p.Hq, h, q0);
-  load_tile<D>(sdO, p.dout, b, p.Sq, p.Hq, h, q0);
-  for (int r = threadIdx.x; r < kT; r += kThreads) {
-    const bool in = q0 + r < p.Sq;
-    cv.lse[r] = in ? p.lse[(size_t(b) * p.Hq + h) * p.Sq + q0 + r] : 0.f;
-    cv.dsum[r] = in ? p.dsum[(size_t(b) * p.Hq + h) * p.Sq + q0 + r] : 0.f;
-  }
-  // keys any row of the tile may see
-  int kend = Lb;
-  if (p.causal) kend = min(kend, min(q0 + kT, p.Sq) - 1 + p.Sk - p.Sq + 1);
-  const int ntiles = kend > 0 ? (kend + kT - 1) / kT : 0;
+  const int diag = p.Sk - p.Sq;               // causal: query i sees keys j <= i + diag
+  const int nq = (p.Sq + kBQ - 1) / kBQ;
+  // causal: the first query that sees key k0 is k0 - diag
+  const int qfirst = p.causal ? max(0, k0 - diag) / kBQ : 0;
+  const int nqe = (k0 < Lb && qfirst < nq) ? nq - qfirst : 0;
+  const int n = p.G * nqe;
 
-  wm::fragment<wm::accumulator, 16, 16, 16, float> acc[D / 16];
-#pragma unroll
-  for (int n = 0; n < D / 16; ++n) wm::fill_fragment(acc[n], 0.f);
-  const __nv_bfloat16* qw = sQ + warp * 16 * Smem<D>::kLd;
-  const __nv_bfloat16* dow = sdO + warp * 16 * Smem<D>::kLd;
-  for (int kt = 0; kt < ntiles; ++kt) {
-    __syncthreads();
-    load_tile<D>(sK, p.k, b, p.Sk, p.Hkv, kvh, kt * kT);
-    load_tile<D>(sV, p.v, b, p.Sk, p.Hkv, kvh, kt * kT);
-    __syncthreads();
-    mm_abt<D>(cv.s, Smem<D>::kLdS, qw, sK);      // S = Q K^T
-    mm_abt<D>(cv.dp, Smem<D>::kLdS, dow, sV);    // dP = dO V^T
-    __syncwarp();
-    for (int e = lane; e < 16 * kT; e += 32) {
-      const int r = e >> 6, c = e & 63;
-      const int i = q0 + warp * 16 + r, j = kt * kT + c;
-      const bool ok = i < p.Sq && j < Lb && (!p.causal || j <= i + p.Sk - p.Sq);
-      const float pr = ok ? __expf(cv.s[r * Smem<D>::kLdS + c] * p.scale - cv.lse[warp * 16 + r]) : 0.f;
-      cv.x[r * (kT + 8) + c] =
-          __float2bfloat16_rn(pr * (cv.dp[r * Smem<D>::kLdS + c] - cv.dsum[warp * 16 + r]));
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(qd_full(s), 1);
+      mbar_init(qd_empty(s), 1);
     }
-    __syncwarp();
-    mm_acc<D>(acc, cv.x, sK);                    // dQ += dS K
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 4);        // one arrival per elementwise warp
+    mbar_init(done, 1);
+    mbar_init(drain, 1);
+    mbar_init(row_full(0), 4);
+    mbar_init(row_full(1), 4);
+    *abort_flag = 0;
+    fence_mbar_init();
+    fence_proxy_async_smem();
   }
-  store_rows<D>(acc, cv.s, p.scale, p.dq, b, p.Sq, p.Hq, h, q0 + warp * 16);
-}
+  if (warp == kWarpMMA) {
+    tmem_alloc(smem_u32(tmem_slot), L::kTmCols);
+    tmem_relinquish();
+  }
+  if (warp == kWarpTMA && lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmDO);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-template <int D>
-__global__ void __launch_bounds__(kThreads) dkdv_kernel(const Params p) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  Carve<D> cv(smem, warp);
-  __nv_bfloat16 *sK = cv.t[0], *sV = cv.t[1], *sQ = cv.t[2], *sdO = cv.t[3];
-  const int k0 = blockIdx.x * kT, kvh = blockIdx.y, b = blockIdx.z;
-  const int Lb = key_len(p, b);
-  load_tile<D>(sK, p.k, b, p.Sk, p.Hkv, kvh, k0);
-  load_tile<D>(sV, p.v, b, p.Sk, p.Hkv, kvh, k0);
-  // query rows that may see one of these keys: causal i >= k0 - (Sk - Sq)
-  const int qfirst = (p.causal ? max(0, k0 - (p.Sk - p.Sq)) : 0) / kT;
-  const int nq = (p.Sq + kT - 1) / kT;
-  const bool any_key = k0 < Lb;
-
-  wm::fragment<wm::accumulator, 16, 16, 16, float> dk[D / 16], dv[D / 16];
+  if (warp == kWarpTMA) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0 && n > 0) {
+      mbar_arrive_expect_tx(kv_full, 2u * L::kTileBytes);
+      for (int hh = 0; hh < L::kHalves; ++hh) {
+        tma_load_4d(base + L::kOffK + hh * kHalfBytes, &tmK, kv_full, hh * 64, kvh, k0, b);
+        tma_load_4d(base + L::kOffV + hh * kHalfBytes, &tmV, kv_full, hh * 64, kvh, k0, b);
+      }
+      bool ok = true;
+      int it = 0;
+      for (; it < n; ++it) {
+        const int s = it % S;
+        const int h = kvh * p.G + it / nqe;
+        const int q0 = (qfirst + it % nqe) * kBQ;
+        ok = mbar_wait(qd_empty(s), ((it / S) & 1) ^ 1, abort_flag, to);
+        if (!ok) break;
+        mbar_arrive_expect_tx(qd_full(s), 2u * L::kTileBytes);
+        for (int hh = 0; hh < L::kHalves; ++hh) {
+          tma_load_4d(base + L::kOffQ + s * L::kTileBytes + hh * kHalfBytes, &tmQ, qd_full(s), hh * 64, h, q0,
+                      b);
+          tma_load_4d(base + L::kOffDO + s * L::kTileBytes + hh * kHalfBytes, &tmDO, qd_full(s), hh * 64, h,
+                      q0, b);
+        }
+      }
+      if (!ok) {
+        volatile int no_abort = 0;
+        for (int i2 = it > S ? it - S : 0; i2 < it; ++i2)
+          mbar_wait(qd_full(i2 % S), (i2 / S) & 1, &no_abort, 200000000ull);
+        mbar_wait(kv_full, 0, &no_abort, 200000000ull);
+      }
+    }
+  } else if (warp == kWarpMMA) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0 && n > 0) {
+      const uint32_t idesc_s = make_idesc_bf16(128, kBQ, 0, 0);   // K/V (A), Q/dO K-major (B)
+      const uint32_t idesc_o = make_idesc_bf16(128, D, 0, 1);     // P^T/dS^T in TMEM, dO/Q MN-major
+      bool ok = mbar_wait(kv_full, 0, abort_flag, to);
+      if (ok) {
+        tc_fence_after();
+        if constexpr (L::kKVInTmem) {
+          copy_tile_to_tmem<D>(tmem + L::kTmK, base + L::kOffK);
+          copy_tile_to_tmem<D>(tmem + L::kTmV, base + L::kOffV);
+        }
+      }
+      for (int it = 0; ok && it <= n; ++it) {
+        if (it < n) ok = mbar_wait(qd_full(it % S), (it / S) & 1, abort_flag, to);
+        if (ok && it > 0) ok = mbar_wait(p_full, (it - 1) & 1, abort_flag, to);
+        if (!ok) break;
+        tc_fence_after();
+        if (it > 0) {
+          const int sp = (it - 1) % S;
+          const uint32_t qa = base + L::kOffQ + sp * L::kTileBytes;
+          const uint32_t da = base + L::kOffDO + sp * L::kTileBytes;
 #pragma unroll
-  for (int n = 0; n < D / 16; ++n) {
-    wm::fill_fragment(dk[n], 0.f);
-    wm::fill_fragment(dv[n], 0.f);
-  }
-  const __nv_bfloat16* kw = sK + warp * 16 * Smem<D>::kLd;
-  const __nv_bfloat16* vw = sV + warp * 16 * Smem<D>::kLd;
-  for (int g = 0; any_key && g < p.G; ++g) {
-    const int h = kvh * p.G + g;
-    for (int qt = qfirst; qt < nq; ++qt) {
-      __syncthreads();
-      load_tile<D>(sQ, p.q, b, p.Sq, p.Hq, h, qt * kT);
-      load_tile<D>(sdO, p.dout, b, p.Sq, p.Hq, h, qt * kT);
-      for (int r = threadIdx.x; r < kT; r += kThreads) {
-        const bool in = qt * kT + r < p.Sq;
-        cv.lse[r] = in ? p.lse[(size_t(b) * p.Hq + h) * p.Sq + qt * kT + r] : 0.f;
-        cv.dsum[r] = in ? p.dsum[(size_t(b) * p.Hq + h) * p.Sq + qt * kT + r] : 0.f;
+          for (int ks = 0; ks < kBQ / 16; ++ks)     // dV += P^T dO
+            umma_ts(tmem + L::kTmDV, tmem + L::kTmS + uint32_t(ks) * 8u, desc_mnmajor<D>(da, ks), idesc_o,
+                    (it > 1 || ks > 0) ? 1u : 0u);
+#pragma unroll
+          for (int ks = 0; ks < kBQ / 16; ++ks)     // dK += dS^T Q
+            umma_ts(tmem + L::kTmDK, tmem + L::kTmP + uint32_t(ks) * 8u, desc_mnmajor<D>(qa, ks), idesc_o,
+                    (it > 1 || ks > 0) ? 1u : 0u);
+          umma_commit(qd_empty(sp));
+          if (it == n) umma_commit(done);
+        }
+        if (it < n) {
+          const int s = it % S;
+          const uint32_t qa = base + L::kOffQ + s * L::kTileBytes;
+          const uint32_t da = base + L::kOffDO + s * L::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {     // S^T = K Q^T
+            if constexpr (L::kKVInTmem)
+              umma_ts(tmem + L::kTmS, tmem + L::kTmK + uint32_t(ks) * 8u, desc_kmajor(qa, ks), idesc_s,
+                      ks > 0 ? 1u : 0u);
+            else
+              umma_ss(tmem + L::kTmS, desc_kmajor(base + L::kOffK, ks), desc_kmajor(qa, ks), idesc_s,
+                      ks > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {     // dP^T = V dO^T
+            if constexpr (L::kKVInTmem)
+              umma_ts(tmem + L::kTmP, tmem + L::kTmV + uint32_t(ks) * 8u, desc_kmajor(da, ks), idesc_s,
+                      ks > 0 ? 1u : 0u);
+            else
+              umma_ss(tmem + L::kTmP, desc_kmajor(base + L::kOffV, ks), desc_kmajor(da, ks), idesc_s,
+                      ks > 0 ? 1u : 0u);
+          }
+          umma_commit(s_full);
+        }
       }
-      __syncthreads();
-      mm_abt<D>(cv.s, Smem<D>::kLdS, kw, sQ);     // S^T = K Q^T (keys x queries)
-      mm_abt<D>(cv.dp, Smem<D>::kLdS, vw, sdO);   // dP^T = V dO^T
-      __syncwarp();
-      for (int e = lane; e < 16 * kT; e += 32) {
-        const int r = e >> 6, c = e & 63;
-        const int j = k0 + warp * 16 + r, i = qt * kT + c;
-        const bool ok = i < p.Sq && j < Lb && (!p.causal || j <= i + p.Sk - p.Sq);
-        const float pr = ok ? __expf(cv.s[r * Smem<D>::kLdS + c] * p.scale - cv.lse[c]) : 0.f;
-        cv.x[r * (kT + 8) + c] = __float2bfloat16_rn(pr);
-        cv.y[r * (kT + 8) + c] = __float2bfloat16_rn(pr * (cv.dp[r * Smem<D>::kLdS + c] - cv.dsum[c]));
+      if (!ok) {
+        volatile int no_abort = 0;
+        umma_commit(drain);
+        mbar_wait(drain, 0, &no_abort, 200000000ull);
       }
+    }
+  } else {
+    // ------------------------------------------------- elementwise + epilogue
+    const int r = warp * 32 + lane;                     // key row = TMEM lane
+    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    const int j = k0 + r;
+    const bool key_ok = j < Lb;
+    const float cl = p.scale_log2;
+    bool aborted = false;
+    for (int it = 0; it < n; ++it) {
+      const int h = kvh * p.G + it / nqe;
+      const int q0 = (qfirst + it % nqe) * kBQ;
+      const int buf = it & 1;
+      float* lrow = rowv + buf * 2 * kBQ;
+      float* drow = lrow + kBQ;
+      {
+        // this tile's query rows: lse (as log2) and Dsum, one per thread;
+        // buffer `buf` was last read two iterations ago, before every warp's
+        // arrival on row_full for the previous iteration
+        const int i = q0 + r;
+        const size_t ri = (size_t(b) * p.Hq + h) * p.Sq + i;
+        lrow[r] = i < p.Sq ? p.lse[ri] * kLog2e : 0.f;
+        drow[r] = i < p.Sq ? p.dsum[ri] : 0.f;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(row_full(buf));
+      }
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(row_full(buf), (it >> 1) & 1, abort_flag, to) &&
+                                                 mbar_wait(s_full, it & 1, abort_flag, to));
+      if (!ok) {
+        aborted = true;
+        break;
+      }
+      tc_fence_after();
+      // admissible query columns c of this key row: lo <= c < hi
+      int lo = 0, hi = min(kBQ, p.Sq - q0);
+      if (p.causal) lo = max(0, j - diag - q0);
+      if (!key_ok) lo = kBQ;
+      const bool full = __all_sync(0xffffffffu, lo == 0 && hi == kBQ);
+#pragma unroll
+      for (int c = 0; c < kBQ / 32; ++c) {
+        uint32_t sv[32], dp[32], pw[16], dw[16];
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(c) * 32u, sv);
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(c) * 32u, dp);
+        tmem_ld_wait_x32(sv);
+        tmem_ld_wait_x32(dp);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int c0 = c * 32 + 2 * e;
+          const float2 l2 = *reinterpret_cast<const float2*>(lrow + c0);
+          const float2 d2 = *reinterpret_cast<const float2*>(drow + c0);
+          const bool ok0 = full || (c0 >= lo && c0 < hi);
+          const bool ok1 = full || (c0 + 1 >= lo && c0 + 1 < hi);
+          float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), cl, -l2.x));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), cl, -l2.y));
+          p0 = ok0 ? p0 : 0.f;
+          p1 = ok1 ? p1 : 0.f;
+          const float s0 = ok0 ? p0 * (__uint_as_float(dp[2 * e]) - d2.x) : 0.f;
+          const float s1 = ok1 ? p1 * (__uint_as_float(dp[2 * e + 1]) - d2.y) : 0.f;
+          pw[e] = pack_bf16x2(p0, p1);
+          dw[e] = pack_bf16x2(s0, s1);
+        }
+        tmem_st_32x32b_x16(tmem + lane_base + L::kTmS + uint32_t(c) * 16u, pw);
+        tmem_st_32x32b_x16(tmem + lane_base + L::kTmP + uint32_t(c) * 16u, dw);
+      }
+      tmem_st_wait();
+      tc_fence_before();
       __syncwarp();
-      mm_acc<D>(dv, cv.x, sdO);                   // dV += P^T dO
-      mm_acc<D>(dk, cv.y, sQ);                    // dK += dS^T Q
+      if (lane == 0) mbar_arrive(p_full);
+    }
+    if (j < p.Sk) {
+      __nv_bfloat16* vrow = p.dv + ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D;
+      __nv_bfloat16* krow = p.dk + ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D;
+      if (n == 0) {
+        store_zero_row(vrow, D);             // no query sees these keys
+        store_zero_row(krow, D);
+      }
+    }
+    if (n > 0 && !aborted) {
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, to));
+      tc_fence_after();
+      if (ok) {
+        __nv_bfloat16* vrow = p.dv + ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D;
+        __nv_bfloat16* krow = p.dk + ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDV + uint32_t(c), v);
+          tmem_ld_wait_x32(v);
+          if (j < p.Sk) store_row32(vrow + c, v, 1.f);
+          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDK + uint32_t(c), v);
+          tmem_ld_wait_x32(v);
+          if (j < p.Sk) store_row32(krow + c, v, p.scale);
+        }
+      }
     }
   }
-  store_rows<D>(dk, cv.s, p.scale, p.dk, b, p.Sk, p.Hkv, kvh, k0 + warp * 16);
-  store_rows<D>(dv, cv.s, 1.f, p.dv, b, p.Sk, p.Hkv, kvh, k0 + warp * 16);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kWarpMMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::kTmCols);
+  }
 }
 
 }  // namespace bwd

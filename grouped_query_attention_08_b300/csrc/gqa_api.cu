@@ -240,29 +240,47 @@ static_assert(gqa::decode::RingF8::kBytes >= sizeof(float) * (gqa::decode::kWarp
 
 template <int D>
 bool bwd_smem_attr_set(int dev) {
+  namespace bw = gqa::bwd;
   static bool done[kMaxDevices] = {false};
   if (dev >= 0 && dev < kMaxDevices && done[dev]) return true;
-  constexpr int bytes = int(gqa::bwd::Smem<D>::kBytes);
-  if (cudaFuncSetAttribute(gqa::bwd::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(gqa::bwd::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
-          cudaSuccess)
+  if (cudaFuncSetAttribute(bw::dq_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(bw::DqLayout<D>::kSmemAlloc)) != cudaSuccess ||
+      cudaFuncSetAttribute(bw::dkdv_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           int(bw::KvLayout<D>::kSmemAlloc)) != cudaSuccess)
     return false;
   if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
   return true;
 }
 
 // Dsum, then dQ and dK/dV (independent of each other) on one stream.
+// q, out, dout [B, Sq, Hq, D]; k, v [B, Sk, Hkv, D] (bf16).
 template <int D>
-int launch_bwd(const gqa::bwd::Params& p, cudaStream_t stream) {
+int launch_bwd(gqa::bwd::Params p, const void* q, const void* k, const void* v, cudaStream_t stream) {
   namespace bw = gqa::bwd;
+  const int Mq = 128 / p.G;
+  p.Mq = Mq;
+  p.n_qt = (p.Sq + Mq - 1) / Mq;
+  p.n_kt = (p.Sk + bw::kBN - 1) / bw::kBN;
+  p.scale_log2 = p.scale * kLog2e;
+  p.timeout_ns = wait_timeout_ns();
+  // dq_kernel: Q / dO tiles of Mq tokens x G heads (row = token * G + head),
+  // K / V tiles of 128 keys; dkdv_kernel: Q / dO tiles of 128 tokens of one
+  // head, K / V tiles of 128 keys.
+  CUtensorMap tmQg, tmDOg, tmQ1, tmDO1, tmK, tmV;
+  if (!encode_4d_bf16(&tmQg, q, D, p.Hq, p.Sq, p.B, 64, p.G, Mq, 1) ||
+      !encode_4d_bf16(&tmDOg, p.dout, D, p.Hq, p.Sq, p.B, 64, p.G, Mq, 1) ||
+      !encode_4d_bf16(&tmQ1, q, D, p.Hq, p.Sq, p.B, 64, 1, bw::kBQ, 1) ||
+      !encode_4d_bf16(&tmDO1, p.dout, D, p.Hq, p.Sq, p.B, 64, 1, bw::kBQ, 1) ||
+      !encode_4d_bf16(&tmK, k, D, p.Hkv, p.Sk, p.B, 64, 1, bw::kBN, 1) ||
+      !encode_4d_bf16(&tmV, v, D, p.Hkv, p.Sk, p.B, 64, 1, bw::kBN, 1))
+    return GQA_ERR_CUDA;
   if (!bwd_smem_attr_set<D>(current_device())) return GQA_ERR_CUDA;
   const long long rows = (long long)p.B * p.Hq * p.Sq;
   bw::dsum_kernel<D><<<unsigned((rows + 7) / 8), 256, 0, stream>>>(p);
-  const dim3 gq((p.Sq + bw::kT - 1) / bw::kT, p.Hq, p.B);
-  bw::dq_kernel<D><<<gq, bw::kThreads, bw::Smem<D>::kBytes, stream>>>(p);
-  const dim3 gk((p.Sk + bw::kT - 1) / bw::kT, p.Hkv, p.B);
-  bw::dkdv_kernel<D><<<gk, bw::kThreads, bw::Smem<D>::kBytes, stream>>>(p);
+  const dim3 gq(unsigned(p.n_qt), unsigned(p.Hkv), unsigned(p.B));
+  bw::dq_kernel<D><<<gq, bw::kThreads, bw::DqLayout<D>::kSmemAlloc, stream>>>(tmQg, tmDOg, tmK, tmV, p);
+  const dim3 gk(unsigned(p.n_kt), unsigned(p.Hkv), unsigned(p.B));
+  bw::dkdv_kernel<D><<<gk, bw::kThreads, bw::KvLayout<D>::kSmemAlloc, stream>>>(tmK, tmV, tmQ1, tmDO1, p);
   return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
 }
 
@@ -672,10 +690,8 @@ int gqa_bwd(const void* q, const void* k, const void* v, const void* out, const 
   if (Hq > 65535 || B > 65535 || (long long)Hq * D * Sq * B > (1LL << 40) ||
       (long long)Hkv * D * Sk * B > (1LL << 40))
     return GQA_ERR_UNSUPPORTED;
+  if (Hq / Hkv > 128) return GQA_ERR_UNSUPPORTED;        // a 128-row tile holds one token of every head
   gqa::bwd::Params p{};
-  p.q = static_cast<const __nv_bfloat16*>(q);
-  p.k = static_cast<const __nv_bfloat16*>(k);
-  p.v = static_cast<const __nv_bfloat16*>(v);
   p.o = static_cast<const __nv_bfloat16*>(out);
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   p.lse = lse;
@@ -693,7 +709,7 @@ int gqa_bwd(const void* q, const void* k, const void* v, const void* out, const 
   p.causal = causal;
   p.scale = scale;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  return D == 64 ? launch_bwd<64>(p, st) : launch_bwd<128>(p, st);
+  return D == 64 ? launch_bwd<64>(p, q, k, v, st) : launch_bwd<128>(p, q, k, v, st);
 }
 
 int gqa_device_status(void* stream) {
