@@ -24,9 +24,10 @@
 //    and every query tile of 128, S^T = K Q^T and dP^T = V dO^T into TMEM,
 //    P^T and dS^T written back over them, dV += P^T dO and dK += dS^T Q
 //    accumulated in TMEM over the whole loop (the group sum).
-// Warp roles (192 threads): warps 0-3 one TMEM lane (tile row) per thread for
-// the elementwise step and the epilogue, warp 4 TMA producer, warp 5 MMA
-// issuer.  Tiles arrive by TMA with the 128-byte swizzle; operands that stay
+// Warp roles (320 threads): warps 0-7 the elementwise step and the epilogue,
+// one TMEM lane (tile row) per thread and warp w taking columns of half w / 4
+// of the row (two warps per SM sub-partition), warp 8 TMA producer, warp 9
+// MMA issuer.  Tiles arrive by TMA with the 128-byte swizzle; operands that stay
 // fixed for the whole CTA (Q and dO in dq_kernel, K and V in dkdv_kernel at
 // D = 64) are copied into TMEM with tcgen05.cp and read from there as the A
 // operand, which leaves the shared-memory operand bandwidth to the streamed
@@ -39,9 +40,10 @@
 namespace gqa {
 namespace bwd {
 
-constexpr int kThreads = 192;
-constexpr int kWarpTMA = 4;
-constexpr int kWarpMMA = 5;
+constexpr int kThreads = 320;
+constexpr int kEwWarps = 8;              // elementwise warps: two per TMEM lane quarter
+constexpr int kWarpTMA = 8;
+constexpr int kWarpMMA = 9;
 constexpr int kBN = 128;                 // keys per tile (dq_kernel); keys per CTA (dkdv_kernel)
 constexpr int kBQ = 128;                 // queries per tile (dkdv_kernel)
 constexpr uint32_t kHalfBytes = 128u * 128u;   // 128 rows x 64 bf16 (128 bytes), one swizzle span
@@ -77,22 +79,37 @@ DEVI int key_len(const Params& p, int b) {
   return L;
 }
 
-// Dsum_i = dO_i . O_i, one warp per (b, h, i).
+// Dsum_i = dO_i . O_i: D / 8 consecutive threads per (b, h, i) row, each
+// with one 16-byte load of dO and of O, reduced by shuffles.
 template <int D>
 __global__ void __launch_bounds__(256) dsum_kernel(const Params p) {
-  const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (row >= (long long)p.B * p.Hq * p.Sq) return;
-  const int i = int(row % p.Sq);
-  const int h = int((row / p.Sq) % p.Hq);
-  const int b = int(row / ((long long)p.Sq * p.Hq));
-  const size_t off = ((size_t(b) * p.Sq + i) * p.Hq + h) * D;
+  constexpr int kTpr = D / 8;                     // threads per row (8 or 16)
+  const long long nrows = (long long)p.B * p.Hq * p.Sq;
+  const long long t = (long long)blockIdx.x * 256 + threadIdx.x;
+  const long long row = t / kTpr;                 // row = (b * Sq + i) * Hq + h: memory order
+  const int part = int(t % kTpr);
   float acc = 0.f;
-  for (int d = lane; d < D; d += 32)
-    acc += __bfloat162float(p.dout[off + d]) * __bfloat162float(p.o[off + d]);
+  if (row < nrows) {
+    const uint4 a = *reinterpret_cast<const uint4*>(p.dout + size_t(row) * D + part * 8);
+    const uint4 o = *reinterpret_cast<const uint4*>(p.o + size_t(row) * D + part * 8);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, ov[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
-  for (int s = 16; s > 0; s >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, s);
-  if (lane == 0) p.dsum[row] = acc;
+    for (int e = 0; e < 4; ++e) {
+      const float2 fa = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&av[e]));
+      const float2 fo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ov[e]));
+      acc = fmaf(fa.x, fo.x, acc);
+      acc = fmaf(fa.y, fo.y, acc);
+    }
+  }
+#pragma unroll
+  for (int sh = kTpr / 2; sh > 0; sh >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sh);
+  if (row < nrows && part == 0) {
+    const int h = int(row % p.Hq);
+    const long long bi = row / p.Hq;              // b * Sq + i
+    const int i = int(bi % p.Sq);
+    const int b = int(bi / p.Sq);
+    p.dsum[(size_t(b) * p.Hq + h) * p.Sq + i] = acc;
+  }
 }
 
 // Shared-memory operand descriptors of a swizzled 128-row tile stored as
@@ -115,6 +132,11 @@ DEVI void copy_tile_to_tmem(uint32_t tcol, uint32_t tile) {
 #pragma unroll
   for (int ks = 0; ks < D / 16; ++ks) tmem_cp_128x256b(tcol + uint32_t(ks) * 8u, desc_kmajor(tile, ks));
 }
+
+// TMEM column of 16-key step ks of a bf16 operand written over a 128-column
+// fp32 tile: the elementwise warp of half h writes keys [64h, 64h + 64) as
+// bf16 pairs into columns [64h, 64h + 32).
+DEVI uint32_t packed_col(int ks) { return uint32_t(ks / 4) * 64u + uint32_t(ks % 4) * 8u; }
 
 // Writes 32 fp32 values times `mul` as bf16 to dst (16-byte aligned).
 DEVI void store_row32(__nv_bfloat16* dst, const uint32_t* v, float mul) {
@@ -149,7 +171,7 @@ struct DqLayout {
   static constexpr uint32_t kOffAbort = kOffSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
   static constexpr uint32_t kSmemAlloc = kBytes + 1024u;
-  // TMEM: S [0,128) (dS over its first 64 as bf16 pairs), dP [128,256),
+  // TMEM: S [0,128) (dS as bf16 pairs in [0,32) and [64,96)), dP [128,256),
   // Q [256, 256+D/2), dO [256+D/2, 256+D), dQ [256+D, 256+2D)
   static constexpr uint32_t kTmS = 0, kTmP = 128, kTmQ = 256, kTmDO = 256 + D / 2, kTmDQ = 256 + D;
   static constexpr uint32_t kTmCols = 512;
@@ -168,7 +190,7 @@ struct KvLayout {
   static constexpr uint32_t kOffV = kTileBytes;
   static constexpr uint32_t kOffQ = 2 * kTileBytes;
   static constexpr uint32_t kOffDO = kOffQ + kStages * kTileBytes;
-  static constexpr uint32_t kOffRow = kOffDO + kStages * kTileBytes;   // [2][2][128] fp32: lse*log2e, Dsum
+  static constexpr uint32_t kOffRow = kOffDO + kStages * kTileBytes;   // [2][2][128] fp32: -lse*log2e, -Dsum
   static constexpr uint32_t kOffBar = kOffRow + 2u * 2u * kBQ * 4u;
   // kv_full, qd_full[S], qd_empty[S], s_full, p_full, done, drain, row_full[2]
   static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2;
@@ -176,8 +198,9 @@ struct KvLayout {
   static constexpr uint32_t kOffAbort = kOffSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
   static constexpr uint32_t kSmemAlloc = kBytes + 1024u;
-  // TMEM: S^T [0,128) (P^T over its first 64), dP^T [128,256) (dS^T over its
-  // first 64), dV [256, 256+D), dK [256+D, 256+2D), and at D = 64 K, V.
+  // TMEM: S^T [0,128) (P^T as bf16 pairs in [0,32) and [64,96)), dP^T
+  // [128,256) (dS^T likewise), dV [256, 256+D), dK [256+D, 256+2D), and at
+  // D = 64 K, V.
   static constexpr uint32_t kTmS = 0, kTmP = 128, kTmDV = 256, kTmDK = 256 + D;
   static constexpr uint32_t kTmK = 256 + 2 * D, kTmV = 256 + 2 * D + D / 2;
   static constexpr uint32_t kTmCols = 512;
@@ -227,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(kv_empty(s), 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 4);        // one arrival per elementwise warp
+    mbar_init(p_full, kEwWarps);   // one arrival per elementwise warp
     mbar_init(done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -303,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t ka = base + L::kOffK + sp * L::kTileBytes;
 #pragma unroll
           for (int ks = 0; ks < kBN / 16; ++ks)
-            umma_ts(tmem + L::kTmDQ, tmem + L::kTmS + uint32_t(ks) * 8u, desc_mnmajor<D>(ka, ks), idesc_q,
+            umma_ts(tmem + L::kTmDQ, tmem + L::kTmS + packed_col(ks), desc_mnmajor<D>(ka, ks), idesc_q,
                     (j > 1 || ks > 0) ? 1u : 0u);
           umma_commit(kv_empty(sp));
           if (j == n) umma_commit(done);
@@ -331,8 +354,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------- elementwise + epilogue
-    const int r = warp * 32 + lane;                     // tile row = TMEM lane
-    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), columns of half w / 4
+    const int r = (warp & 3) * 32 + lane;
+    const int half = warp >> 2;
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const int token = r / p.G, gg = r - token * p.G;
     const int i = q0 + token;
     const bool row_ok = r < p.G * p.Mq && i < p.Sq;
@@ -345,7 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       dsum = p.dsum[rowidx];
       hi_row = p.causal ? min(Lb, i + diag + 1) : Lb;
     }
-    const float cl = p.scale_log2;
+    const uint64_t cl2 = f2_pack(p.scale_log2, p.scale_log2);
+    const uint64_t nl2 = f2_pack(-lse2, -lse2);
+    const uint64_t nd2 = f2_pack(-dsum, -dsum);
     bool aborted = false;
     for (int j = 0; j < n; ++j) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, to));
@@ -354,48 +381,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int lim = hi_row - j * kBN;
-      const bool full = __all_sync(0xffffffffu, lim >= kBN || !row_ok);
+      // this warp's 64 keys of the tile: [half * 64, half * 64 + 64)
+      const int lim = hi_row - j * kBN - half * 64;
+      const bool full = __all_sync(0xffffffffu, lim >= 64 || !row_ok);
+      uint32_t sv[64], dp[64], ds[32];
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u, sv);
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u + 32u, sv + 32);
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u, dp);
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u + 32u, dp + 32);
+      tmem_ld_wait_x32(sv);
+      tmem_ld_wait_x32(sv + 32);
+      tmem_ld_wait_x32(dp);
+      tmem_ld_wait_x32(dp + 32);
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
-        uint32_t sv[32], dp[32], ds[16];
-        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(c) * 32u, sv);
-        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(c) * 32u, dp);
-        tmem_ld_wait_x32(sv);
-        tmem_ld_wait_x32(dp);
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int k0 = c * 32 + 2 * e;
-          const bool ok0 = full ? row_ok : (k0 < lim);
-          const bool ok1 = full ? row_ok : (k0 + 1 < lim);
-          const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), cl, -lse2));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), cl, -lse2));
-          const float d0 = ok0 ? p0 * (__uint_as_float(dp[2 * e]) - dsum) : 0.f;
-          const float d1 = ok1 ? p1 * (__uint_as_float(dp[2 * e + 1]) - dsum) : 0.f;
-          ds[e] = pack_bf16x2(d0, d1);
+      for (int e = 0; e < 32; ++e) {
+        const int k0 = 2 * e;
+        float x0, x1, p0, p1, t0, t1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), cl2, nl2), x0, x1);
+        p0 = ex2_approx(x0);
+        p1 = ex2_approx(x1);
+        if (!full) {
+          p0 = (k0 < lim) ? p0 : 0.f;
+          p1 = (k0 + 1 < lim) ? p1 : 0.f;
         }
-        tmem_st_32x32b_x16(tmem + lane_base + L::kTmS + uint32_t(c) * 16u, ds);
+        f2_unpack(f2_add(f2_pack(__uint_as_float(dp[k0]), __uint_as_float(dp[k0 + 1])), nd2), t0, t1);
+        ds[e] = pack_bf16x2(p0 * t0, p1 * t1);
       }
+      // dS (bf16 pairs) over the start of this half's own S columns (the
+      // other warp of these lanes may still be reading its half)
+      tmem_st_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u, ds);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    __nv_bfloat16* drow = p.dq + ((size_t(b) * p.Sq + i) * p.Hq + h) * D;
+    __nv_bfloat16* drow = p.dq + ((size_t(b) * p.Sq + i) * p.Hq + h) * D + half * (D / 2);
     if (n > 0 && !aborted) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, to));
       tc_fence_after();
       if (ok) {
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < D / 2; c += 32) {
           uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDQ + uint32_t(c), v);
+          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDQ + uint32_t(half * (D / 2) + c), v);
           tmem_ld_wait_x32(v);
           if (row_ok) store_row32(drow + c, v, p.scale);
         }
       }
     } else if (n == 0 && row_ok) {
-      store_zero_row(drow, D);               // no admissible key: dQ = 0
+      store_zero_row(drow, D / 2);           // no admissible key: dQ = 0
     }
   }
 
@@ -432,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto row_full = [&](int i) { return bar(5 + 2 * S + i); };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffSlot);
-  float* rowv = reinterpret_cast<float*>(sbase + L::kOffRow);   // [2][2][kBQ]: lse * log2(e), Dsum
+  float* rowv = reinterpret_cast<float*>(sbase + L::kOffRow);   // [2][2][kBQ]: -lse * log2(e), -Dsum
   const uint64_t to = p.timeout_ns;
 
   const int kvh = blockIdx.y, b = blockIdx.z;
@@ -452,11 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(qd_empty(s), 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 4);        // one arrival per elementwise warp
+    mbar_init(p_full, kEwWarps);   // one arrival per elementwise warp
     mbar_init(done, 1);
     mbar_init(drain, 1);
-    mbar_init(row_full(0), 4);
-    mbar_init(row_full(1), 4);
+    mbar_init(row_full(0), kEwWarps);
+    mbar_init(row_full(1), kEwWarps);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -531,11 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t da = base + L::kOffDO + sp * L::kTileBytes;
 #pragma unroll
           for (int ks = 0; ks < kBQ / 16; ++ks)     // dV += P^T dO
-            umma_ts(tmem + L::kTmDV, tmem + L::kTmS + uint32_t(ks) * 8u, desc_mnmajor<D>(da, ks), idesc_o,
+            umma_ts(tmem + L::kTmDV, tmem + L::kTmS + packed_col(ks), desc_mnmajor<D>(da, ks), idesc_o,
                     (it > 1 || ks > 0) ? 1u : 0u);
 #pragma unroll
           for (int ks = 0; ks < kBQ / 16; ++ks)     // dK += dS^T Q
-            umma_ts(tmem + L::kTmDK, tmem + L::kTmP + uint32_t(ks) * 8u, desc_mnmajor<D>(qa, ks), idesc_o,
+            umma_ts(tmem + L::kTmDK, tmem + L::kTmP + packed_col(ks), desc_mnmajor<D>(qa, ks), idesc_o,
                     (it > 1 || ks > 0) ? 1u : 0u);
           umma_commit(qd_empty(sp));
           if (it == n) umma_commit(done);
@@ -573,29 +607,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------- elementwise + epilogue
-    const int r = warp * 32 + lane;                     // key row = TMEM lane
-    const uint32_t lane_base = uint32_t(warp * 32) << 16;
+    // warp w: TMEM lanes 32 (w % 4) .. +31 (key rows), query columns of half w / 4
+    const int r = (warp & 3) * 32 + lane;
+    const int half = warp >> 2;
+    const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const int j = k0 + r;
     const bool key_ok = j < Lb;
-    const float cl = p.scale_log2;
+    const uint64_t cl2 = f2_pack(p.scale_log2, p.scale_log2);
     bool aborted = false;
     for (int it = 0; it < n; ++it) {
       const int h = kvh * p.G + it / nqe;
       const int q0 = (qfirst + it % nqe) * kBQ;
       const int buf = it & 1;
-      float* lrow = rowv + buf * 2 * kBQ;
-      float* drow = lrow + kBQ;
-      {
-        // this tile's query rows: lse (as log2) and Dsum, one per thread;
-        // buffer `buf` was last read two iterations ago, before every warp's
-        // arrival on row_full for the previous iteration
+      float* nlrow = rowv + buf * 2 * kBQ;     // -lse * log2(e) of the tile's query rows
+      float* ndrow = nlrow + kBQ;              // -Dsum
+      // Warps 0-3 fill buffer `buf` (one query row per thread).  It was last
+      // read two iterations ago, before every warp's arrival on row_full for
+      // the previous iteration, which the writers have waited for.
+      if (half == 0) {
         const int i = q0 + r;
         const size_t ri = (size_t(b) * p.Hq + h) * p.Sq + i;
-        lrow[r] = i < p.Sq ? p.lse[ri] * kLog2e : 0.f;
-        drow[r] = i < p.Sq ? p.dsum[ri] : 0.f;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(row_full(buf));
+        nlrow[r] = i < p.Sq ? -p.lse[ri] * kLog2e : 0.f;
+        ndrow[r] = i < p.Sq ? -p.dsum[ri] : 0.f;
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(row_full(buf));
       const bool ok = __all_sync(0xffffffffu, mbar_wait(row_full(buf), (it >> 1) & 1, abort_flag, to) &&
                                                  mbar_wait(s_full, it & 1, abort_flag, to));
       if (!ok) {
@@ -603,65 +639,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // admissible query columns c of this key row: lo <= c < hi
-      int lo = 0, hi = min(kBQ, p.Sq - q0);
-      if (p.causal) lo = max(0, j - diag - q0);
-      if (!key_ok) lo = kBQ;
-      const bool full = __all_sync(0xffffffffu, lo == 0 && hi == kBQ);
+      // admissible query columns c (within this half) of this key row: lo <= c < hi
+      const int qh = q0 + half * 64;
+      int lo = 0;
+      const int hi = min(64, p.Sq - qh);
+      if (p.causal) lo = max(0, j - diag - qh);
+      if (!key_ok) lo = 64;
+      const bool full = __all_sync(0xffffffffu, lo == 0 && hi == 64);
+      uint32_t sv[64], dp[64], pw[32], dw[32];
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u, sv);
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u + 32u, sv + 32);
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u, dp);
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u + 32u, dp + 32);
+      tmem_ld_wait_x32(sv);
+      tmem_ld_wait_x32(sv + 32);
+      tmem_ld_wait_x32(dp);
+      tmem_ld_wait_x32(dp + 32);
+      const float* nl = nlrow + half * 64;
+      const float* nd = ndrow + half * 64;
 #pragma unroll
-      for (int c = 0; c < kBQ / 32; ++c) {
-        uint32_t sv[32], dp[32], pw[16], dw[16];
-        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(c) * 32u, sv);
-        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(c) * 32u, dp);
-        tmem_ld_wait_x32(sv);
-        tmem_ld_wait_x32(dp);
+      for (int e = 0; e < 16; ++e) {
+        const float4 l4 = *reinterpret_cast<const float4*>(nl + 4 * e);
+        const float4 d4 = *reinterpret_cast<const float4*>(nd + 4 * e);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c0 = c * 32 + 2 * e;
-          const float2 l2 = *reinterpret_cast<const float2*>(lrow + c0);
-          const float2 d2 = *reinterpret_cast<const float2*>(drow + c0);
-          const bool ok0 = full || (c0 >= lo && c0 < hi);
-          const bool ok1 = full || (c0 + 1 >= lo && c0 + 1 < hi);
-          float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * e]), cl, -l2.x));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * e + 1]), cl, -l2.y));
-          p0 = ok0 ? p0 : 0.f;
-          p1 = ok1 ? p1 : 0.f;
-          const float s0 = ok0 ? p0 * (__uint_as_float(dp[2 * e]) - d2.x) : 0.f;
-          const float s1 = ok1 ? p1 * (__uint_as_float(dp[2 * e + 1]) - d2.y) : 0.f;
-          pw[e] = pack_bf16x2(p0, p1);
-          dw[e] = pack_bf16x2(s0, s1);
+        for (int u = 0; u < 2; ++u) {
+          const int c0 = 4 * e + 2 * u;
+          float x0, x1, p0, p1, t0, t1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])), cl2,
+                           u ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y)),
+                    x0, x1);
+          p0 = ex2_approx(x0);
+          p1 = ex2_approx(x1);
+          if (!full) {
+            p0 = (c0 >= lo && c0 < hi) ? p0 : 0.f;
+            p1 = (c0 + 1 >= lo && c0 + 1 < hi) ? p1 : 0.f;
+          }
+          f2_unpack(f2_add(f2_pack(__uint_as_float(dp[c0]), __uint_as_float(dp[c0 + 1])),
+                           u ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y)),
+                    t0, t1);
+          pw[c0 / 2] = pack_bf16x2(p0, p1);
+          dw[c0 / 2] = pack_bf16x2(p0 * t0, p1 * t1);
         }
-        tmem_st_32x32b_x16(tmem + lane_base + L::kTmS + uint32_t(c) * 16u, pw);
-        tmem_st_32x32b_x16(tmem + lane_base + L::kTmP + uint32_t(c) * 16u, dw);
       }
+      // P^T and dS^T (bf16 pairs) over the start of this half's own columns
+      tmem_st_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u, pw);
+      tmem_st_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u, dw);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    if (j < p.Sk) {
-      __nv_bfloat16* vrow = p.dv + ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D;
-      __nv_bfloat16* krow = p.dk + ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D;
-      if (n == 0) {
-        store_zero_row(vrow, D);             // no query sees these keys
-        store_zero_row(krow, D);
-      }
+    // this warp's half of the key row: columns [half * D/2, half * D/2 + D/2)
+    const size_t orow = ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D + size_t(half) * (D / 2);
+    if (n == 0 && j < p.Sk) {
+      store_zero_row(p.dv + orow, D / 2);    // no query sees these keys
+      store_zero_row(p.dk + orow, D / 2);
     }
     if (n > 0 && !aborted) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, to));
       tc_fence_after();
       if (ok) {
-        __nv_bfloat16* vrow = p.dv + ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D;
-        __nv_bfloat16* krow = p.dk + ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D;
 #pragma unroll
-        for (int c = 0; c < D; c += 32) {
+        for (int c = 0; c < D / 2; c += 32) {
           uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDV + uint32_t(c), v);
+          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDV + uint32_t(half * (D / 2) + c), v);
           tmem_ld_wait_x32(v);
-          if (j < p.Sk) store_row32(vrow + c, v, 1.f);
-          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDK + uint32_t(c), v);
+          if (j < p.Sk) store_row32(p.dv + orow + c, v, 1.f);
+          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDK + uint32_t(half * (D / 2) + c), v);
           tmem_ld_wait_x32(v);
-          if (j < p.Sk) store_row32(krow + c, v, p.scale);
+          if (j < p.Sk) store_row32(p.dk + orow + c, v, p.scale);
         }
       }
     }

@@ -275,8 +275,8 @@ int launch_bwd(gqa::bwd::Params p, const void* q, const void* k, const void* v, 
       !encode_4d_bf16(&tmV, v, D, p.Hkv, p.Sk, p.B, 64, 1, bw::kBN, 1))
     return GQA_ERR_CUDA;
   if (!bwd_smem_attr_set<D>(current_device())) return GQA_ERR_CUDA;
-  const long long rows = (long long)p.B * p.Hq * p.Sq;
-  bw::dsum_kernel<D><<<unsigned((rows + 7) / 8), 256, 0, stream>>>(p);
+  const long long dsum_threads = (long long)p.B * p.Hq * p.Sq * (D / 8);
+  bw::dsum_kernel<D><<<unsigned((dsum_threads + 255) / 256), 256, 0, stream>>>(p);
   const dim3 gq(unsigned(p.n_qt), unsigned(p.Hkv), unsigned(p.B));
   bw::dq_kernel<D><<<gq, bw::kThreads, bw::DqLayout<D>::kSmemAlloc, stream>>>(tmQg, tmDOg, tmK, tmV, p);
   const dim3 gk(unsigned(p.n_kt), unsigned(p.Hkv), unsigned(p.B));
