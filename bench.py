@@ -334,6 +334,45 @@ def time_decode_fp8(gqa, name, device, flush, reps=20, warmup=3):
                 w.name, w.B, w.Hq, w.Hkv, w.D, w.Smax, w.lens[0], w.lens[1])}
 
 
+def time_backward(gqa, name, device, flush, reps=10, warmup=3):
+    """Per-call time of gqa_bwd (Dsum, dQ, dK/dV kernels) on a named dense
+    prefill workload, with the forward's out and lse as inputs and a seeded
+    N(0,1) upstream gradient; L2 flushed before every call.  Returns TFLOP/s
+    of algorithmic work (10 * D flops per admissible pair)."""
+    w = inputs.WORKLOADS[name]
+    inp = inputs.make_workload(w)
+    d = {k: (v.to(device) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    g = torch.Generator("cpu").manual_seed(w.seed + 101)
+    dout = torch.randn(tuple(d["q"].shape), generator=g, dtype=torch.float32).to(torch.bfloat16).to(device)
+    out, lse = gqa.gqa_fwd(d["q"], d["k"], d["v"], causal=w.causal, seqlens_k=d["seqlens_k"], scale=w.scale)
+    lens = None if inp["seqlens_k"] is None else inp["seqlens_k"].tolist()
+    flops = roofline.backward_flops(w.B, w.Hq, w.Sq, w.Sk, w.D, w.causal, lens)
+    dq, dk, dv = torch.empty_like(d["q"]), torch.empty_like(d["k"]), torch.empty_like(d["v"])
+    dsum = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=device)
+
+    def call():
+        gqa.gqa_bwd(d["q"], d["k"], d["v"], out, dout, lse, causal=w.causal, seqlens_k=d["seqlens_k"],
+                    scale=w.scale, dq=dq, dk=dk, dv=dv, dsum=dsum)
+
+    for _ in range(warmup):
+        flush.fill_(1)
+        call()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        evs[i][0].record()
+        call()
+        evs[i][1].record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / reps
+    tf = flops / (ms * 1e-3) / 1e12
+    peaks, psrc = _peaks()
+    peak = peaks["bf16_tflops"]
+    return {"tflops": tf, "ms": ms, "frac": tf / peak, "peak_tflops": peak, "peak_source": psrc + " bf16 burst",
+            "workload": "backward of " + _workload_name(w), "algorithmic_flops_per_launch": flops,
+            "launches_per_call": 3}
+
+
 def _workload_name(w):
     if isinstance(w, inputs.SparseWorkload):
         return "%s: %s under a block mask, %d-token blocks, band of +-%d blocks plus key block 0" % (
@@ -360,6 +399,9 @@ def main():
     ap.add_argument("--no-other-workloads", action="store_true",
                     help="skip timing the other prefill workloads after the main run")
     ap.add_argument("--other-reps", type=int, default=10)
+    ap.add_argument("--backward-workloads", default="bert_base,causal_long",
+                    help="comma-separated dense prefill workloads whose backward (gqa_bwd) is timed after "
+                         "the main run; empty for none")
     ap.add_argument("--other-workloads",
                     default="bert_base,bert_large_long,causal_long,bert_base_varlen,bert_large_long_sparse,"
                             "llama_decode_fp8",
@@ -518,6 +560,13 @@ def main():
         torch.cuda.synchronize()
         if gqa.gqa_device_status() != 0:
             raise RuntimeError("device error while timing the other prefill workloads")
+    bwd = {}
+    if not args.no_other_workloads:
+        for name in [n for n in args.backward_workloads.split(",") if n]:
+            bwd[name] = time_backward(gqa, name, device, flush, reps=args.other_reps)
+        torch.cuda.synchronize()
+        if gqa.gqa_device_status() != 0:
+            raise RuntimeError("device error while timing the backward")
 
     cb = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -544,6 +593,7 @@ def main():
             "cpu_baseline": cb,
             "prefill_workloads": others,
             "decode_fp8": dec8,
+            "backward": bwd,
         }
         print(json.dumps(line))
     if ws > 1:

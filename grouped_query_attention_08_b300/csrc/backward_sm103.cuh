@@ -165,17 +165,22 @@ struct DqLayout {
   static constexpr uint32_t kOffK = 2 * kTileBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, kv_full[S], kv_empty[S], s_full, p_full, done, drain
-  static constexpr int kNumBars = 1 + 2 * kStages + 4;
+  // q_full, kv_full[S], kv_empty[S], s_full, p_full, done, drain, sd_read, dq_done
+  static constexpr int kNumBars = 1 + 2 * kStages + 6;
   static constexpr uint32_t kOffSlot = kOffBar + 8u * kNumBars;
   static constexpr uint32_t kOffAbort = kOffSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
   static constexpr uint32_t kSmemAlloc = kBytes + 1024u;
-  // TMEM: S [0,128) (dS as bf16 pairs in [0,32) and [64,96)), dP [128,256),
-  // Q [256, 256+D/2), dO [256+D/2, 256+D), dQ [256+D, 256+2D)
+  // TMEM: S [0,128), dP [128,256), Q [256, 256+D/2), dO [256+D/2, 256+D),
+  // dQ [256+D, 256+2D).  dS (bf16 pairs): D = 64 in its own columns
+  // [384, 448), so that S and dP are free as soon as they have been read;
+  // D = 128 over dP, half h's 64 keys in [128 + 64h, 128 + 64h + 32).
+  static constexpr bool kSepDS = (D == 64);
   static constexpr uint32_t kTmS = 0, kTmP = 128, kTmQ = 256, kTmDO = 256 + D / 2, kTmDQ = 256 + D;
+  static constexpr uint32_t kTmDS = 256 + 2 * D;
   static constexpr uint32_t kTmCols = 512;
   static_assert(kTmDQ + D <= kTmCols, "TMEM column map overflows");
+  static_assert(!kSepDS || kTmDS + 64 <= kTmCols, "TMEM column map overflows");
   static_assert(kSmemAlloc > 116u * 1024u, "one CTA per SM: its TMEM allocation takes all 512 columns");
 };
 
@@ -192,15 +197,16 @@ struct KvLayout {
   static constexpr uint32_t kOffDO = kOffQ + kStages * kTileBytes;
   static constexpr uint32_t kOffRow = kOffDO + kStages * kTileBytes;   // [2][2][128] fp32: -lse*log2e, -Dsum
   static constexpr uint32_t kOffBar = kOffRow + 2u * 2u * kBQ * 4u;
-  // kv_full, qd_full[S], qd_empty[S], s_full, p_full, done, drain, row_full[2]
-  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2;
+  // kv_full, qd_full[S], qd_empty[S], s_full, p_full, done, drain, row_full[2], sd_read
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 + 1;
   static constexpr uint32_t kOffSlot = kOffBar + 8u * kNumBars;
   static constexpr uint32_t kOffAbort = kOffSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
   static constexpr uint32_t kSmemAlloc = kBytes + 1024u;
-  // TMEM: S^T [0,128) (P^T as bf16 pairs in [0,32) and [64,96)), dP^T
-  // [128,256) (dS^T likewise), dV [256, 256+D), dK [256+D, 256+2D), and at
-  // D = 64 K, V.
+  // TMEM: S^T [0,128), dP^T [128,256), dV [256, 256+D), dK [256+D, 256+2D),
+  // and at D = 64 K, V.  The bf16 pairs of half h's 64 query columns go over
+  // that half's dP^T columns: dS^T in [128 + 64h, +32), P^T in
+  // [128 + 64h + 32, +32); S^T is free as soon as it has been read.
   static constexpr uint32_t kTmS = 0, kTmP = 128, kTmDV = 256, kTmDK = 256 + D;
   static constexpr uint32_t kTmK = 256 + 2 * D, kTmV = 256 + 2 * D + D / 2;
   static constexpr uint32_t kTmCols = 512;
@@ -210,10 +216,16 @@ struct KvLayout {
 };
 
 // dQ for one 128-row tile (Mq tokens x G heads of K/V head kvh, batch b).
-// Per key tile j the issuer runs S(j) = Q K(j)^T and dP(j) = dO V(j)^T, the
-// elementwise warps turn them into dS(j) (bf16 over S), then the issuer runs
-// dQ += dS(j) K(j) followed by S(j+1), dP(j+1) (in issue order, so S(j+1)
-// overwrites dS(j) only after it has been read).
+// Schedule over the key tiles j (one issuing thread, so the tensor core runs
+// its MMAs in issue order):
+//   issuer:      S(0), dP(0); then per j: once the elementwise warps have read
+//                S(j) and dP(j): S(j+1) (and dP(j+1) when dS has its own
+//                columns); once dS(j) is written: dQ += dS(j) K(j) (then
+//                dP(j+1) when dS lies over dP)
+//   elementwise: per j: read S(j), dP(j); signal; dS(j) = P (dP - Dsum) in
+//                registers; write dS(j) (its own columns: after dQ(j-1) has
+//                read dS(j-1)); signal
+// so S(j+1) is computed while the elementwise warps work on tile j.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
@@ -231,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto kv_full = [&](int s) { return bar(1 + s); };
   auto kv_empty = [&](int s) { return bar(1 + S + s); };
   const uint32_t s_full = bar(1 + 2 * S), p_full = bar(2 + 2 * S), done = bar(3 + 2 * S), drain = bar(4 + 2 * S);
+  const uint32_t sd_read = bar(5 + 2 * S), dq_done = bar(6 + 2 * S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffSlot);
   const uint64_t to = p.timeout_ns;
@@ -253,6 +266,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(p_full, kEwWarps);   // one arrival per elementwise warp
     mbar_init(done, 1);
     mbar_init(drain, 1);
+    mbar_init(sd_read, kEwWarps);
+    mbar_init(dq_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -309,43 +324,62 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n > 0) {
       const uint32_t idesc_s = make_idesc_bf16(128, kBN, 0, 0);   // A in TMEM, B K-major
       const uint32_t idesc_q = make_idesc_bf16(128, D, 0, 1);     // dS in TMEM, K MN-major
-      bool ok = mbar_wait(q_full, 0, abort_flag, to);
+      auto issue_s = [&](int jj) {          // S(jj) = Q K(jj)^T
+        const uint32_t ka = base + L::kOffK + (jj % S) * L::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ts(tmem + L::kTmS, tmem + L::kTmQ + uint32_t(ks) * 8u, desc_kmajor(ka, ks), idesc_s,
+                  ks > 0 ? 1u : 0u);
+      };
+      auto issue_dp = [&](int jj) {         // dP(jj) = dO V(jj)^T
+        const uint32_t va = base + L::kOffV + (jj % S) * L::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ts(tmem + L::kTmP, tmem + L::kTmDO + uint32_t(ks) * 8u, desc_kmajor(va, ks), idesc_s,
+                  ks > 0 ? 1u : 0u);
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, to) && mbar_wait(kv_full(0), 0, abort_flag, to);
       if (ok) {
         tc_fence_after();
         copy_tile_to_tmem<D>(tmem + L::kTmQ, base + L::kOffQ);
         copy_tile_to_tmem<D>(tmem + L::kTmDO, base + L::kOffDO);
+        issue_s(0);
+        issue_dp(0);
+        umma_commit(s_full);
       }
-      for (int j = 0; ok && j <= n; ++j) {
-        if (j < n) ok = mbar_wait(kv_full(j % S), (j / S) & 1, abort_flag, to);
-        if (ok && j > 0) ok = mbar_wait(p_full, (j - 1) & 1, abort_flag, to);
+      for (int j = 0; ok && j < n; ++j) {
+        const bool more = j + 1 < n;
+        // S(j) and dP(j) have been read: S(j+1) (and dP(j+1)) may overwrite them
+        ok = mbar_wait(sd_read, j & 1, abort_flag, to);
+        if (ok && more) ok = mbar_wait(kv_full((j + 1) % S), ((j + 1) / S) & 1, abort_flag, to);
         if (!ok) break;
         tc_fence_after();
-        if (j > 0) {
-          // dQ += dS(j-1) K(j-1)
-          const int sp = (j - 1) % S;
-          const uint32_t ka = base + L::kOffK + sp * L::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < kBN / 16; ++ks)
-            umma_ts(tmem + L::kTmDQ, tmem + L::kTmS + packed_col(ks), desc_mnmajor<D>(ka, ks), idesc_q,
-                    (j > 1 || ks > 0) ? 1u : 0u);
-          umma_commit(kv_empty(sp));
-          if (j == n) umma_commit(done);
+        if (more) {
+          issue_s(j + 1);
+          if constexpr (L::kSepDS) {
+            issue_dp(j + 1);
+            umma_commit(s_full);
+          }
         }
-        if (j < n) {
-          const int s = j % S;
-          const uint32_t ka = base + L::kOffK + s * L::kTileBytes;
-          const uint32_t va = base + L::kOffV + s * L::kTileBytes;
+        ok = mbar_wait(p_full, j & 1, abort_flag, to);
+        if (!ok) break;
+        tc_fence_after();
+        // dQ += dS(j) K(j)
+        const uint32_t ka = base + L::kOffK + (j % S) * L::kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            umma_ts(tmem + L::kTmS, tmem + L::kTmQ + uint32_t(ks) * 8u, desc_kmajor(ka, ks), idesc_s,
-                    ks > 0 ? 1u : 0u);
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks)
-            umma_ts(tmem + L::kTmP, tmem + L::kTmDO + uint32_t(ks) * 8u, desc_kmajor(va, ks), idesc_s,
-                    ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < kBN / 16; ++ks) {
+          const uint32_t acol = L::kSepDS ? L::kTmDS + uint32_t(ks) * 8u : L::kTmP + packed_col(ks);
+          umma_ts(tmem + L::kTmDQ, tmem + acol, desc_mnmajor<D>(ka, ks), idesc_q, (j > 0 || ks > 0) ? 1u : 0u);
+        }
+        umma_commit(kv_empty(j % S));
+        if constexpr (L::kSepDS) {
+          umma_commit(dq_done);
+        } else if (more) {
+          issue_dp(j + 1);                  // dP(j+1) over dS(j), after dQ has read it
           umma_commit(s_full);
         }
       }
+      if (ok) umma_commit(done);
       if (!ok) {
         volatile int no_abort = 0;
         umma_commit(drain);
@@ -354,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------- elementwise + epilogue
-    // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), columns of half w / 4
+    // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), keys of half w / 4
     const int r = (warp & 3) * 32 + lane;
     const int half = warp >> 2;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
@@ -373,9 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t cl2 = f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t nl2 = f2_pack(-lse2, -lse2);
     const uint64_t nd2 = f2_pack(-dsum, -dsum);
+    // where this half's dS goes (bf16 pairs, 32 columns)
+    const uint32_t ds_col = L::kSepDS ? L::kTmDS + uint32_t(half) * 32u : L::kTmP + uint32_t(half) * 64u;
     bool aborted = false;
     for (int j = 0; j < n; ++j) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, to));
+      bool ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, to));
       if (!ok) {
         aborted = true;
         break;
@@ -393,6 +429,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait_x32(sv + 32);
       tmem_ld_wait_x32(dp);
       tmem_ld_wait_x32(dp + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sd_read);
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
         const int k0 = 2 * e;
@@ -407,9 +446,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         f2_unpack(f2_add(f2_pack(__uint_as_float(dp[k0]), __uint_as_float(dp[k0 + 1])), nd2), t0, t1);
         ds[e] = pack_bf16x2(p0 * t0, p1 * t1);
       }
-      // dS (bf16 pairs) over the start of this half's own S columns (the
-      // other warp of these lanes may still be reading its half)
-      tmem_st_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u, ds);
+      if (L::kSepDS && j > 0) {
+        // dQ(j-1) must have read dS(j-1) before it is overwritten
+        ok = __all_sync(0xffffffffu, mbar_wait(dq_done, (j - 1) & 1, abort_flag, to));
+        if (!ok) {
+          aborted = true;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st_32x32b_x32(tmem + lane_base + ds_col, ds);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -442,10 +488,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // dK and dV for 128 keys of K/V head kvh, batch b.  Iteration it covers head
-// kvh * G + it / nqe of the group and query tile qfirst + it % nqe: the
-// issuer runs S^T = K Q^T and dP^T = V dO^T, the elementwise warps write
-// P^T and dS^T (bf16) over them, then the issuer runs dV += P^T dO and
-// dK += dS^T Q followed by the next iteration's S^T and dP^T.
+// kvh * G + it / nqe of the group and query tile qfirst + it % nqe.
+//   issuer:      S^T(0), dP^T(0); then per it: once the elementwise warps
+//                have read S^T(it) and dP^T(it): S^T(it+1); once P^T(it) and
+//                dS^T(it) are written (over dP^T): dV += P^T dO, dK += dS^T Q,
+//                then dP^T(it+1) (issue order keeps it behind their reads)
+//   elementwise: per it: read S^T(it), dP^T(it); signal; P^T, dS^T in
+//                registers; write them over dP^T; signal
+// so S^T(it+1) is computed while the elementwise warps work on iteration it.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -464,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto qd_empty = [&](int s) { return bar(1 + S + s); };
   const uint32_t s_full = bar(1 + 2 * S), p_full = bar(2 + 2 * S), done = bar(3 + 2 * S), drain = bar(4 + 2 * S);
   auto row_full = [&](int i) { return bar(5 + 2 * S + i); };
+  const uint32_t sd_read = bar(7 + 2 * S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffSlot);
   float* rowv = reinterpret_cast<float*>(sbase + L::kOffRow);   // [2][2][kBQ]: -lse * log2(e), -Dsum
@@ -491,6 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(row_full(0), kEwWarps);
     mbar_init(row_full(1), kEwWarps);
+    mbar_init(sd_read, kEwWarps);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -546,59 +598,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n > 0) {
       const uint32_t idesc_s = make_idesc_bf16(128, kBQ, 0, 0);   // K/V (A), Q/dO K-major (B)
       const uint32_t idesc_o = make_idesc_bf16(128, D, 0, 1);     // P^T/dS^T in TMEM, dO/Q MN-major
-      bool ok = mbar_wait(kv_full, 0, abort_flag, to);
+      auto issue_st = [&](int t) {          // S^T(t) = K Q(t)^T
+        const uint32_t qa = base + L::kOffQ + (t % S) * L::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          if constexpr (L::kKVInTmem)
+            umma_ts(tmem + L::kTmS, tmem + L::kTmK + uint32_t(ks) * 8u, desc_kmajor(qa, ks), idesc_s,
+                    ks > 0 ? 1u : 0u);
+          else
+            umma_ss(tmem + L::kTmS, desc_kmajor(base + L::kOffK, ks), desc_kmajor(qa, ks), idesc_s,
+                    ks > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_dpt = [&](int t) {         // dP^T(t) = V dO(t)^T
+        const uint32_t da = base + L::kOffDO + (t % S) * L::kTileBytes;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          if constexpr (L::kKVInTmem)
+            umma_ts(tmem + L::kTmP, tmem + L::kTmV + uint32_t(ks) * 8u, desc_kmajor(da, ks), idesc_s,
+                    ks > 0 ? 1u : 0u);
+          else
+            umma_ss(tmem + L::kTmP, desc_kmajor(base + L::kOffV, ks), desc_kmajor(da, ks), idesc_s,
+                    ks > 0 ? 1u : 0u);
+        }
+      };
+      bool ok = mbar_wait(kv_full, 0, abort_flag, to) && mbar_wait(qd_full(0), 0, abort_flag, to);
       if (ok) {
         tc_fence_after();
         if constexpr (L::kKVInTmem) {
           copy_tile_to_tmem<D>(tmem + L::kTmK, base + L::kOffK);
           copy_tile_to_tmem<D>(tmem + L::kTmV, base + L::kOffV);
         }
+        issue_st(0);
+        issue_dpt(0);
+        umma_commit(s_full);
       }
-      for (int it = 0; ok && it <= n; ++it) {
-        if (it < n) ok = mbar_wait(qd_full(it % S), (it / S) & 1, abort_flag, to);
-        if (ok && it > 0) ok = mbar_wait(p_full, (it - 1) & 1, abort_flag, to);
+      for (int it = 0; ok && it < n; ++it) {
+        const bool more = it + 1 < n;
+        ok = mbar_wait(sd_read, it & 1, abort_flag, to);
+        if (ok && more) ok = mbar_wait(qd_full((it + 1) % S), ((it + 1) / S) & 1, abort_flag, to);
         if (!ok) break;
         tc_fence_after();
-        if (it > 0) {
-          const int sp = (it - 1) % S;
-          const uint32_t qa = base + L::kOffQ + sp * L::kTileBytes;
-          const uint32_t da = base + L::kOffDO + sp * L::kTileBytes;
+        if (more) issue_st(it + 1);
+        ok = mbar_wait(p_full, it & 1, abort_flag, to);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t qa = base + L::kOffQ + (it % S) * L::kTileBytes;
+        const uint32_t da = base + L::kOffDO + (it % S) * L::kTileBytes;
 #pragma unroll
-          for (int ks = 0; ks < kBQ / 16; ++ks)     // dV += P^T dO
-            umma_ts(tmem + L::kTmDV, tmem + L::kTmS + packed_col(ks), desc_mnmajor<D>(da, ks), idesc_o,
-                    (it > 1 || ks > 0) ? 1u : 0u);
+        for (int ks = 0; ks < kBQ / 16; ++ks)       // dV += P^T dO
+          umma_ts(tmem + L::kTmDV, tmem + L::kTmP + 32u + packed_col(ks), desc_mnmajor<D>(da, ks), idesc_o,
+                  (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
-          for (int ks = 0; ks < kBQ / 16; ++ks)     // dK += dS^T Q
-            umma_ts(tmem + L::kTmDK, tmem + L::kTmP + packed_col(ks), desc_mnmajor<D>(qa, ks), idesc_o,
-                    (it > 1 || ks > 0) ? 1u : 0u);
-          umma_commit(qd_empty(sp));
-          if (it == n) umma_commit(done);
-        }
-        if (it < n) {
-          const int s = it % S;
-          const uint32_t qa = base + L::kOffQ + s * L::kTileBytes;
-          const uint32_t da = base + L::kOffDO + s * L::kTileBytes;
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {     // S^T = K Q^T
-            if constexpr (L::kKVInTmem)
-              umma_ts(tmem + L::kTmS, tmem + L::kTmK + uint32_t(ks) * 8u, desc_kmajor(qa, ks), idesc_s,
-                      ks > 0 ? 1u : 0u);
-            else
-              umma_ss(tmem + L::kTmS, desc_kmajor(base + L::kOffK, ks), desc_kmajor(qa, ks), idesc_s,
-                      ks > 0 ? 1u : 0u);
-          }
-#pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {     // dP^T = V dO^T
-            if constexpr (L::kKVInTmem)
-              umma_ts(tmem + L::kTmP, tmem + L::kTmV + uint32_t(ks) * 8u, desc_kmajor(da, ks), idesc_s,
-                      ks > 0 ? 1u : 0u);
-            else
-              umma_ss(tmem + L::kTmP, desc_kmajor(base + L::kOffV, ks), desc_kmajor(da, ks), idesc_s,
-                      ks > 0 ? 1u : 0u);
-          }
+        for (int ks = 0; ks < kBQ / 16; ++ks)       // dK += dS^T Q
+          umma_ts(tmem + L::kTmDK, tmem + L::kTmP + packed_col(ks), desc_mnmajor<D>(qa, ks), idesc_o,
+                  (it > 0 || ks > 0) ? 1u : 0u);
+        umma_commit(qd_empty(it % S));
+        if (more) {
+          issue_dpt(it + 1);
           umma_commit(s_full);
         }
       }
+      if (ok) umma_commit(done);
       if (!ok) {
         volatile int no_abort = 0;
         umma_commit(drain);
@@ -655,6 +716,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld_wait_x32(sv + 32);
       tmem_ld_wait_x32(dp);
       tmem_ld_wait_x32(dp + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sd_read);
       const float* nl = nlrow + half * 64;
       const float* nd = ndrow + half * 64;
 #pragma unroll
@@ -681,9 +745,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           dw[c0 / 2] = pack_bf16x2(p0 * t0, p1 * t1);
         }
       }
-      // P^T and dS^T (bf16 pairs) over the start of this half's own columns
-      tmem_st_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u, pw);
+      // dS^T and P^T (bf16 pairs) over this half's own dP^T columns
       tmem_st_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u, dw);
+      tmem_st_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u + 32u, pw);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();

@@ -53,6 +53,14 @@ def prefill_flops(B, Hq, Sq, Sk, D, causal, seqlens_k=None) -> int:
     return 4 * D * prefill_pairs(B, Hq, Sq, Sk, causal, seqlens_k)
 
 
+def backward_flops(B, Hq, Sq, Sk, D, causal, seqlens_k=None) -> int:
+    """Algorithmic flops of one backward call: per admissible (query row, key)
+    pair five D-long multiply-adds -- the recomputed score q.k, dP = dO.v, and
+    the three gradient products P dO (dV), dS k (dQ), dS q (dK) -- i.e.
+    10 * D flops, 2.5 times the forward's 4 * D."""
+    return 10 * D * prefill_pairs(B, Hq, Sq, Sk, causal, seqlens_k)
+
+
 def blockmask_pairs(B: int, Hq: int, Sq: int, Sk: int, causal: bool, block_mask, block_size: int,
                     seqlens_k: Optional[Sequence[int]] = None) -> int:
     """Admissible (b, h, i, j) pairs under a block mask [ceil(Sq/bs), ceil(Sk/bs)]
