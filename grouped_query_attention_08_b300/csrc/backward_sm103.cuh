@@ -24,14 +24,14 @@
 //    and every query tile of 128, S^T = K Q^T and dP^T = V dO^T into TMEM,
 //    P^T and dS^T written back over them, dV += P^T dO and dK += dS^T Q
 //    accumulated in TMEM over the whole loop (the group sum).
-// Warp roles (320 threads): warps 0-7 the elementwise step and the epilogue,
-// one TMEM lane (tile row) per thread and warp w taking columns of half w / 4
-// of the row (two warps per SM sub-partition), warp 8 TMA producer, warp 9
-// MMA issuer.  Tiles arrive by TMA with the 128-byte swizzle; operands that stay
-// fixed for the whole CTA (Q and dO in dq_kernel, K and V in dkdv_kernel at
-// D = 64) are copied into TMEM with tcgen05.cp and read from there as the A
-// operand, which leaves the shared-memory operand bandwidth to the streamed
-// tiles.  All waits are bounded: on a timeout the kernel raises a device
+// Warp roles (576 threads): warps 0-15 the elementwise step and the
+// epilogue, one TMEM lane (tile row) per thread and warp w taking the 32
+// columns of group w / 4 of the row (four warps per SM sub-partition, so
+// TMEM-load and MUFU latencies overlap), warp 16 TMA producer, warp 17 MMA
+// issuer.  Tiles arrive by TMA with the 128-byte swizzle; operands that stay
+// fixed for the whole CTA (Q and dO in dq_kernel) are copied into TMEM with
+// tcgen05.cp and read from there as the A operand, which leaves the
+// shared-memory operand bandwidth to the streamed tiles.  All waits are bounded: on a timeout the kernel raises a device
 // error, drains its copies and MMAs, and exits.
 #pragma once
 
@@ -40,10 +40,10 @@
 namespace gqa {
 namespace bwd {
 
-constexpr int kThreads = 320;
-constexpr int kEwWarps = 8;              // elementwise warps: two per TMEM lane quarter
-constexpr int kWarpTMA = 8;
-constexpr int kWarpMMA = 9;
+constexpr int kEwWarps = 16;             // elementwise warps: four per TMEM lane quarter
+constexpr int kThreads = (kEwWarps + 2) * 32;
+constexpr int kWarpTMA = kEwWarps;
+constexpr int kWarpMMA = kEwWarps + 1;
 constexpr int kBN = 128;                 // keys per tile (dq_kernel); keys per CTA (dkdv_kernel)
 constexpr int kBQ = 128;                 // queries per tile (dkdv_kernel)
 constexpr uint32_t kHalfBytes = 128u * 128u;   // 128 rows x 64 bf16 (128 bytes), one swizzle span
@@ -134,9 +134,9 @@ DEVI void copy_tile_to_tmem(uint32_t tcol, uint32_t tile) {
 }
 
 // TMEM column of 16-key step ks of a bf16 operand written over a 128-column
-// fp32 tile: the elementwise warp of half h writes keys [64h, 64h + 64) as
-// bf16 pairs into columns [64h, 64h + 32).
-DEVI uint32_t packed_col(int ks) { return uint32_t(ks / 4) * 64u + uint32_t(ks % 4) * 8u; }
+// fp32 tile: the elementwise warps of column group c hold keys [32c, 32c+32)
+// and write them as bf16 pairs into the first 16 of their own 32 columns.
+DEVI uint32_t packed_col(int ks) { return uint32_t(ks / 2) * 32u + uint32_t(ks % 2) * 8u; }
 
 // Writes 32 fp32 values times `mul` as bf16 to dst (16-byte aligned).
 DEVI void store_row32(__nv_bfloat16* dst, const uint32_t* v, float mul) {
@@ -174,7 +174,7 @@ struct DqLayout {
   // TMEM: S [0,128), dP [128,256), Q [256, 256+D/2), dO [256+D/2, 256+D),
   // dQ [256+D, 256+2D).  dS (bf16 pairs): D = 64 in its own columns
   // [384, 448), so that S and dP are free as soon as they have been read;
-  // D = 128 over dP, half h's 64 keys in [128 + 64h, 128 + 64h + 32).
+  // D = 128 over dP, column group c's 32 keys in [128 + 32c, 128 + 32c + 16).
   static constexpr bool kSepDS = (D == 64);
   static constexpr uint32_t kTmS = 0, kTmP = 128, kTmQ = 256, kTmDO = 256 + D / 2, kTmDQ = 256 + D;
   static constexpr uint32_t kTmDS = 256 + 2 * D;
@@ -190,28 +190,29 @@ struct KvLayout {
   static constexpr int kHalves = D / 64;
   static constexpr uint32_t kTileBytes = kHalves * kHalfBytes;
   static constexpr int kStages = (D == 64) ? 3 : 2;        // Q/dO ring depth
-  static constexpr bool kKVInTmem = (D == 64);             // K, V copied into TMEM as A operands
+  static constexpr int kDPBufs = (D == 64) ? 2 : 1;        // dP^T buffers in TMEM
   static constexpr uint32_t kOffK = 0;
   static constexpr uint32_t kOffV = kTileBytes;
   static constexpr uint32_t kOffQ = 2 * kTileBytes;
   static constexpr uint32_t kOffDO = kOffQ + kStages * kTileBytes;
   static constexpr uint32_t kOffRow = kOffDO + kStages * kTileBytes;   // [2][2][128] fp32: -lse*log2e, -Dsum
   static constexpr uint32_t kOffBar = kOffRow + 2u * 2u * kBQ * 4u;
-  // kv_full, qd_full[S], qd_empty[S], s_full, p_full, done, drain, row_full[2], sd_read
-  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 + 1;
+  // kv_full, qd_full[S], qd_empty[S], s_full, p_full[0], done, drain, row_full[2], sd_read, p_full[1]
+  static constexpr int kNumBars = 1 + 2 * kStages + 4 + 2 + 1 + 1;
   static constexpr uint32_t kOffSlot = kOffBar + 8u * kNumBars;
   static constexpr uint32_t kOffAbort = kOffSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
   static constexpr uint32_t kSmemAlloc = kBytes + 1024u;
-  // TMEM: S^T [0,128), dP^T [128,256), dV [256, 256+D), dK [256+D, 256+2D),
-  // and at D = 64 K, V.  The bf16 pairs of half h's 64 query columns go over
-  // that half's dP^T columns: dS^T in [128 + 64h, +32), P^T in
-  // [128 + 64h + 32, +32); S^T is free as soon as it has been read.
-  static constexpr uint32_t kTmS = 0, kTmP = 128, kTmDV = 256, kTmDK = 256 + D;
-  static constexpr uint32_t kTmK = 256 + 2 * D, kTmV = 256 + 2 * D + D / 2;
+  // TMEM: S^T [0,128), dP^T buffer 0 [128,256), dV [256, 256+D), dK
+  // [256+D, 256+2D), and at D = 64 dP^T buffer 1 [384,512).  The bf16 pairs
+  // of column group c's 32 queries go over that group's columns of the dP^T
+  // buffer they were computed in: dS^T in [+32c, +16), P^T in [+32c+16, +16).
+  // S^T is free as soon as it has been read; with two dP^T buffers the next
+  // iteration's dP^T goes into the other one while dV and dK still read this.
+  static constexpr uint32_t kTmS = 0, kTmDV = 256, kTmDK = 256 + D;
+  static constexpr uint32_t kTmP0 = 128, kTmP1 = (kDPBufs == 2) ? 384 : 128;
   static constexpr uint32_t kTmCols = 512;
-  static_assert(!kKVInTmem || kTmV + D / 2 <= kTmCols, "TMEM column map overflows");
-  static_assert(kKVInTmem || kTmDK + D <= kTmCols, "TMEM column map overflows");
+  static_assert(kTmDK + D <= kTmCols && (kDPBufs == 1 || kTmDK + D <= kTmP1), "TMEM column map overflows");
   static_assert(kSmemAlloc > 116u * 1024u, "one CTA per SM: its TMEM allocation takes all 512 columns");
 };
 
@@ -388,9 +389,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------- elementwise + epilogue
-    // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), keys of half w / 4
+    // warp w: TMEM lanes 32 (w % 4) .. +31 (tile rows), keys of column group w / 4
     const int r = (warp & 3) * 32 + lane;
-    const int half = warp >> 2;
+    const int grp = warp >> 2;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const int token = r / p.G, gg = r - token * p.G;
     const int i = q0 + token;
@@ -407,8 +408,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t cl2 = f2_pack(p.scale_log2, p.scale_log2);
     const uint64_t nl2 = f2_pack(-lse2, -lse2);
     const uint64_t nd2 = f2_pack(-dsum, -dsum);
-    // where this half's dS goes (bf16 pairs, 32 columns)
-    const uint32_t ds_col = L::kSepDS ? L::kTmDS + uint32_t(half) * 32u : L::kTmP + uint32_t(half) * 64u;
+    // where this group's dS goes (bf16 pairs, 16 columns)
+    const uint32_t ds_col = L::kSepDS ? L::kTmDS + uint32_t(grp) * 16u : L::kTmP + uint32_t(grp) * 32u;
     bool aborted = false;
     for (int j = 0; j < n; ++j) {
       bool ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, to));
@@ -417,23 +418,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // this warp's 64 keys of the tile: [half * 64, half * 64 + 64)
-      const int lim = hi_row - j * kBN - half * 64;
-      const bool full = __all_sync(0xffffffffu, lim >= 64 || !row_ok);
-      uint32_t sv[64], dp[64], ds[32];
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u, sv);
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u + 32u, sv + 32);
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u, dp);
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u + 32u, dp + 32);
+      // this warp's 32 keys of the tile: [grp * 32, grp * 32 + 32)
+      const int lim = hi_row - j * kBN - grp * 32;
+      const bool full = __all_sync(0xffffffffu, lim >= 32 || !row_ok);
+      uint32_t sv[32], dp[32], ds[16];
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(grp) * 32u, sv);
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(grp) * 32u, dp);
       tmem_ld_wait_x32(sv);
-      tmem_ld_wait_x32(sv + 32);
       tmem_ld_wait_x32(dp);
-      tmem_ld_wait_x32(dp + 32);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sd_read);
 #pragma unroll
-      for (int e = 0; e < 32; ++e) {
+      for (int e = 0; e < 16; ++e) {
         const int k0 = 2 * e;
         float x0, x1, p0, p1, t0, t1;
         f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), cl2, nl2), x0, x1);
@@ -455,27 +452,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
       }
-      tmem_st_32x32b_x32(tmem + lane_base + ds_col, ds);
+      tmem_st_32x32b_x16(tmem + lane_base + ds_col, ds);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(p_full);
     }
-    __nv_bfloat16* drow = p.dq + ((size_t(b) * p.Sq + i) * p.Hq + h) * D + half * (D / 2);
+    // epilogue: column group grp < D / 32 writes dQ columns [32 grp, 32 grp + 32)
+    __nv_bfloat16* drow = p.dq + ((size_t(b) * p.Sq + i) * p.Hq + h) * D + grp * 32;
     if (n > 0 && !aborted) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, to));
       tc_fence_after();
-      if (ok) {
-#pragma unroll
-        for (int c = 0; c < D / 2; c += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDQ + uint32_t(half * (D / 2) + c), v);
-          tmem_ld_wait_x32(v);
-          if (row_ok) store_row32(drow + c, v, p.scale);
-        }
+      if (ok && grp < D / 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDQ + uint32_t(grp) * 32u, v);
+        tmem_ld_wait_x32(v);
+        if (row_ok) store_row32(drow, v, p.scale);
       }
-    } else if (n == 0 && row_ok) {
-      store_zero_row(drow, D / 2);           // no admissible key: dQ = 0
+    } else if (n == 0 && row_ok && grp < D / 32) {
+      store_zero_row(drow, 32);              // no admissible key: dQ = 0
     }
   }
 
@@ -490,12 +485,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 // dK and dV for 128 keys of K/V head kvh, batch b.  Iteration it covers head
 // kvh * G + it / nqe of the group and query tile qfirst + it % nqe.
 //   issuer:      S^T(0), dP^T(0); then per it: once the elementwise warps
-//                have read S^T(it) and dP^T(it): S^T(it+1); once P^T(it) and
-//                dS^T(it) are written (over dP^T): dV += P^T dO, dK += dS^T Q,
-//                then dP^T(it+1) (issue order keeps it behind their reads)
+//                have read S^T(it) and dP^T(it): S^T(it+1) (and with two dP^T
+//                buffers dP^T(it+1) into the other one); once P^T(it) and
+//                dS^T(it) are written (over dP^T(it)): dV += P^T dO,
+//                dK += dS^T Q (then, with one buffer, dP^T(it+1): issue order
+//                keeps it behind their reads)
 //   elementwise: per it: read S^T(it), dP^T(it); signal; P^T, dS^T in
-//                registers; write them over dP^T; signal
-// so S^T(it+1) is computed while the elementwise warps work on iteration it.
+//                registers; write them over dP^T(it); signal
+// so the next scores are computed while the elementwise warps work on
+// iteration it and, with two buffers, dV and dK overlap the next iteration.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -512,9 +510,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t kv_full = bar(0);
   auto qd_full = [&](int s) { return bar(1 + s); };
   auto qd_empty = [&](int s) { return bar(1 + S + s); };
-  const uint32_t s_full = bar(1 + 2 * S), p_full = bar(2 + 2 * S), done = bar(3 + 2 * S), drain = bar(4 + 2 * S);
+  const uint32_t s_full = bar(1 + 2 * S), done = bar(3 + 2 * S), drain = bar(4 + 2 * S);
   auto row_full = [&](int i) { return bar(5 + 2 * S + i); };
   const uint32_t sd_read = bar(7 + 2 * S);
+  // p_full for iteration it is barrier it & 1: an iteration's arrivals never
+  // meet the previous one's on the same barrier before the issuer has seen it
+  auto p_full = [&](int i) { return i ? bar(8 + 2 * S) : bar(2 + 2 * S); };
+  auto tm_dp = [&](int it) -> uint32_t { return (L::kDPBufs == 2 && (it & 1)) ? L::kTmP1 : L::kTmP0; };
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffSlot);
   float* rowv = reinterpret_cast<float*>(sbase + L::kOffRow);   // [2][2][kBQ]: -lse * log2(e), -Dsum
@@ -537,7 +539,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(qd_empty(s), 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, kEwWarps);   // one arrival per elementwise warp
+    mbar_init(p_full(0), kEwWarps);   // one arrival per elementwise warp
+    mbar_init(p_full(1), kEwWarps);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     mbar_init(row_full(0), kEwWarps);
@@ -601,34 +604,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto issue_st = [&](int t) {          // S^T(t) = K Q(t)^T
         const uint32_t qa = base + L::kOffQ + (t % S) * L::kTileBytes;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          if constexpr (L::kKVInTmem)
-            umma_ts(tmem + L::kTmS, tmem + L::kTmK + uint32_t(ks) * 8u, desc_kmajor(qa, ks), idesc_s,
-                    ks > 0 ? 1u : 0u);
-          else
-            umma_ss(tmem + L::kTmS, desc_kmajor(base + L::kOffK, ks), desc_kmajor(qa, ks), idesc_s,
-                    ks > 0 ? 1u : 0u);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ss(tmem + L::kTmS, desc_kmajor(base + L::kOffK, ks), desc_kmajor(qa, ks), idesc_s,
+                  ks > 0 ? 1u : 0u);
       };
       auto issue_dpt = [&](int t) {         // dP^T(t) = V dO(t)^T
         const uint32_t da = base + L::kOffDO + (t % S) * L::kTileBytes;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          if constexpr (L::kKVInTmem)
-            umma_ts(tmem + L::kTmP, tmem + L::kTmV + uint32_t(ks) * 8u, desc_kmajor(da, ks), idesc_s,
-                    ks > 0 ? 1u : 0u);
-          else
-            umma_ss(tmem + L::kTmP, desc_kmajor(base + L::kOffV, ks), desc_kmajor(da, ks), idesc_s,
-                    ks > 0 ? 1u : 0u);
-        }
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma_ss(tmem + tm_dp(t), desc_kmajor(base + L::kOffV, ks), desc_kmajor(da, ks), idesc_s,
+                  ks > 0 ? 1u : 0u);
       };
       bool ok = mbar_wait(kv_full, 0, abort_flag, to) && mbar_wait(qd_full(0), 0, abort_flag, to);
       if (ok) {
         tc_fence_after();
-        if constexpr (L::kKVInTmem) {
-          copy_tile_to_tmem<D>(tmem + L::kTmK, base + L::kOffK);
-          copy_tile_to_tmem<D>(tmem + L::kTmV, base + L::kOffV);
-        }
         issue_st(0);
         issue_dpt(0);
         umma_commit(s_full);
@@ -639,23 +628,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (ok && more) ok = mbar_wait(qd_full((it + 1) % S), ((it + 1) / S) & 1, abort_flag, to);
         if (!ok) break;
         tc_fence_after();
-        if (more) issue_st(it + 1);
-        ok = mbar_wait(p_full, it & 1, abort_flag, to);
+        if (more) {
+          issue_st(it + 1);
+          if constexpr (L::kDPBufs == 2) {
+            // the other buffer's P^T / dS^T (iteration it-1) were read by
+            // dV / dK issued before this
+            issue_dpt(it + 1);
+            umma_commit(s_full);
+          }
+        }
+        ok = mbar_wait(p_full(it & 1), (it >> 1) & 1, abort_flag, to);
         if (!ok) break;
         tc_fence_after();
         const uint32_t qa = base + L::kOffQ + (it % S) * L::kTileBytes;
         const uint32_t da = base + L::kOffDO + (it % S) * L::kTileBytes;
+        const uint32_t pb = tm_dp(it);
 #pragma unroll
         for (int ks = 0; ks < kBQ / 16; ++ks)       // dV += P^T dO
-          umma_ts(tmem + L::kTmDV, tmem + L::kTmP + 32u + packed_col(ks), desc_mnmajor<D>(da, ks), idesc_o,
+          umma_ts(tmem + L::kTmDV, tmem + pb + 16u + packed_col(ks), desc_mnmajor<D>(da, ks), idesc_o,
                   (it > 0 || ks > 0) ? 1u : 0u);
 #pragma unroll
         for (int ks = 0; ks < kBQ / 16; ++ks)       // dK += dS^T Q
-          umma_ts(tmem + L::kTmDK, tmem + L::kTmP + packed_col(ks), desc_mnmajor<D>(qa, ks), idesc_o,
+          umma_ts(tmem + L::kTmDK, tmem + pb + packed_col(ks), desc_mnmajor<D>(qa, ks), idesc_o,
                   (it > 0 || ks > 0) ? 1u : 0u);
         umma_commit(qd_empty(it % S));
-        if (more) {
-          issue_dpt(it + 1);
+        if (L::kDPBufs == 1 && more) {
+          issue_dpt(it + 1);                // over P^T / dS^T(it), after dV / dK read them
           umma_commit(s_full);
         }
       }
@@ -668,9 +666,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------- elementwise + epilogue
-    // warp w: TMEM lanes 32 (w % 4) .. +31 (key rows), query columns of half w / 4
+    // warp w: TMEM lanes 32 (w % 4) .. +31 (key rows), query columns of group w / 4
     const int r = (warp & 3) * 32 + lane;
-    const int half = warp >> 2;
+    const int grp = warp >> 2;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const int j = k0 + r;
     const bool key_ok = j < Lb;
@@ -685,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // Warps 0-3 fill buffer `buf` (one query row per thread).  It was last
       // read two iterations ago, before every warp's arrival on row_full for
       // the previous iteration, which the writers have waited for.
-      if (half == 0) {
+      if (grp == 0) {
         const int i = q0 + r;
         const size_t ri = (size_t(b) * p.Hq + h) * p.Sq + i;
         nlrow[r] = i < p.Sq ? -p.lse[ri] * kLog2e : 0.f;
@@ -700,29 +698,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // admissible query columns c (within this half) of this key row: lo <= c < hi
-      const int qh = q0 + half * 64;
+      // admissible query columns c (within this group) of this key row: lo <= c < hi
+      const int qg = q0 + grp * 32;
       int lo = 0;
-      const int hi = min(64, p.Sq - qh);
-      if (p.causal) lo = max(0, j - diag - qh);
-      if (!key_ok) lo = 64;
-      const bool full = __all_sync(0xffffffffu, lo == 0 && hi == 64);
-      uint32_t sv[64], dp[64], pw[32], dw[32];
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u, sv);
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(half) * 64u + 32u, sv + 32);
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u, dp);
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u + 32u, dp + 32);
+      const int hi = min(32, p.Sq - qg);
+      if (p.causal) lo = max(0, j - diag - qg);
+      if (!key_ok) lo = 32;
+      const bool full = __all_sync(0xffffffffu, lo == 0 && hi == 32);
+      uint32_t sv[32], dp[32], pw[16], dw[16];
+      const uint32_t pcol = tm_dp(it) + uint32_t(grp) * 32u;   // this group's dP^T columns
+      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(grp) * 32u, sv);
+      tmem_ld_32x32b_x32(tmem + lane_base + pcol, dp);
       tmem_ld_wait_x32(sv);
-      tmem_ld_wait_x32(sv + 32);
       tmem_ld_wait_x32(dp);
-      tmem_ld_wait_x32(dp + 32);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(sd_read);
-      const float* nl = nlrow + half * 64;
-      const float* nd = ndrow + half * 64;
+      const float* nl = nlrow + grp * 32;
+      const float* nd = ndrow + grp * 32;
 #pragma unroll
-      for (int e = 0; e < 16; ++e) {
+      for (int e = 0; e < 8; ++e) {
         const float4 l4 = *reinterpret_cast<const float4*>(nl + 4 * e);
         const float4 d4 = *reinterpret_cast<const float4*>(nd + 4 * e);
 #pragma unroll
@@ -745,34 +740,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           dw[c0 / 2] = pack_bf16x2(p0 * t0, p1 * t1);
         }
       }
-      // dS^T and P^T (bf16 pairs) over this half's own dP^T columns
-      tmem_st_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u, dw);
-      tmem_st_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(half) * 64u + 32u, pw);
+      // dS^T and P^T (bf16 pairs) over this group's own dP^T columns
+      tmem_st_32x32b_x16(tmem + lane_base + pcol, dw);
+      tmem_st_32x32b_x16(tmem + lane_base + pcol + 16u, pw);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(p_full(it & 1));
     }
-    // this warp's half of the key row: columns [half * D/2, half * D/2 + D/2)
-    const size_t orow = ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D + size_t(half) * (D / 2);
-    if (n == 0 && j < p.Sk) {
-      store_zero_row(p.dv + orow, D / 2);    // no query sees these keys
-      store_zero_row(p.dk + orow, D / 2);
+    // epilogue: column group grp < D / 32 writes columns [32 grp, 32 grp + 32)
+    // of the key row's dK and dV
+    const size_t orow = ((size_t(b) * p.Sk + j) * p.Hkv + kvh) * D + size_t(grp) * 32;
+    if (n == 0 && j < p.Sk && grp < D / 32) {
+      store_zero_row(p.dv + orow, 32);       // no query sees these keys
+      store_zero_row(p.dk + orow, 32);
     }
     if (n > 0 && !aborted) {
       const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, to));
       tc_fence_after();
-      if (ok) {
-#pragma unroll
-        for (int c = 0; c < D / 2; c += 32) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDV + uint32_t(half * (D / 2) + c), v);
-          tmem_ld_wait_x32(v);
-          if (j < p.Sk) store_row32(p.dv + orow + c, v, 1.f);
-          tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDK + uint32_t(half * (D / 2) + c), v);
-          tmem_ld_wait_x32(v);
-          if (j < p.Sk) store_row32(p.dk + orow + c, v, p.scale);
-        }
+      if (ok && grp < D / 32) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDV + uint32_t(grp) * 32u, v);
+        tmem_ld_wait_x32(v);
+        if (j < p.Sk) store_row32(p.dv + orow, v, 1.f);
+        tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDK + uint32_t(grp) * 32u, v);
+        tmem_ld_wait_x32(v);
+        if (j < p.Sk) store_row32(p.dk + orow, v, p.scale);
       }
     }
   }
