@@ -165,8 +165,8 @@ struct DqLayout {
   static constexpr uint32_t kOffK = 2 * kTileBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, kv_full[S], kv_empty[S], s_full, p_full, done, drain, sd_read, dq_done
-  static constexpr int kNumBars = 1 + 2 * kStages + 6;
+  // q_full, kv_full[S], kv_empty[S], s_full, p_full, done, drain, sd_read, dq_done, q_empty, dq_free
+  static constexpr int kNumBars = 1 + 2 * kStages + 8;
   static constexpr uint32_t kOffSlot = kOffBar + 8u * kNumBars;
   static constexpr uint32_t kOffAbort = kOffSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
@@ -216,17 +216,20 @@ struct KvLayout {
   static_assert(kSmemAlloc > 116u * 1024u, "one CTA per SM: its TMEM allocation takes all 512 columns");
 };
 
-// dQ for one 128-row tile (Mq tokens x G heads of K/V head kvh, batch b).
-// Schedule over the key tiles j (one issuing thread, so the tensor core runs
-// its MMAs in issue order):
+// dQ, persistent: CTA c takes tiles c, c + gridDim.x, ... of the
+// n_qt * Hkv * B tiles (tile = Mq tokens x G heads of K/V head kvh, batch b;
+// the token block varies fastest, so neighbouring CTAs share K/V in L2).
+// Iteration counters run on across tiles, so the next tile's Q/dO and K/V
+// land while the current one is computed.  Schedule over a tile's key tiles
+// j (one issuing thread: the tensor core runs its MMAs in issue order):
 //   issuer:      S(0), dP(0); then per j: once the elementwise warps have read
 //                S(j) and dP(j): S(j+1) (and dP(j+1) when dS has its own
 //                columns); once dS(j) is written: dQ += dS(j) K(j) (then
-//                dP(j+1) when dS lies over dP)
+//                dP(j+1) when dS lies over dP).  A tile's first dQ waits for
+//                the previous tile's epilogue to have read dQ.
 //   elementwise: per j: read S(j), dP(j); signal; dS(j) = P (dP - Dsum) in
-//                registers; write dS(j) (its own columns: after dQ(j-1) has
-//                read dS(j-1)); signal
-// so S(j+1) is computed while the elementwise warps work on tile j.
+//                registers; write dS(j) (its own columns: after the previous
+//                dQ product has read them); signal.  Then the epilogue.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
@@ -245,20 +248,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto kv_empty = [&](int s) { return bar(1 + S + s); };
   const uint32_t s_full = bar(1 + 2 * S), p_full = bar(2 + 2 * S), done = bar(3 + 2 * S), drain = bar(4 + 2 * S);
   const uint32_t sd_read = bar(5 + 2 * S), dq_done = bar(6 + 2 * S);
+  const uint32_t q_empty = bar(7 + 2 * S), dq_free = bar(8 + 2 * S);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffSlot);
   const uint64_t to = p.timeout_ns;
-
-  const int kvh = blockIdx.y, b = blockIdx.z;
-  const int q0 = blockIdx.x * p.Mq;
-  const int Lb = key_len(p, b);
+  const int n_tiles = p.n_qt * p.Hkv * p.B;
   const int diag = p.Sk - p.Sq;               // causal: query i sees keys j <= i + diag
-  int kmax = Lb;
-  if (p.causal) kmax = min(kmax, min(q0 + p.Mq, p.Sq) - 1 + diag + 1);
-  const int n = kmax > 0 ? (kmax + kBN - 1) / kBN : 0;
+
+  // tile -> (batch, K/V head, first token, key length, number of key tiles)
+  struct Tile {
+    int b, kvh, q0, Lb, n;
+  };
+  auto tile_info = [&](int t) -> Tile {
+    Tile T;
+    const int x = t % p.n_qt;
+    const int rest = t / p.n_qt;
+    T.kvh = rest % p.Hkv;
+    T.b = rest / p.Hkv;
+    T.q0 = x * p.Mq;
+    T.Lb = key_len(p, T.b);
+    int kmax = T.Lb;
+    if (p.causal) kmax = min(kmax, min(T.q0 + p.Mq, p.Sq) - 1 + diag + 1);
+    T.n = kmax > 0 ? (kmax + kBN - 1) / kBN : 0;
+    return T;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < S; ++s) {
       mbar_init(kv_full(s), 1);
       mbar_init(kv_empty(s), 1);
@@ -269,6 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     mbar_init(sd_read, kEwWarps);
     mbar_init(dq_done, 1);
+    mbar_init(dq_free, kEwWarps);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -290,97 +308,121 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------ producer
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       const uint32_t q_bytes = 2u * uint32_t(L::kHalves) * 128u * uint32_t(p.G * p.Mq);
-      mbar_arrive_expect_tx(q_full, q_bytes);
-      for (int hh = 0; hh < L::kHalves; ++hh) {
-        tma_load_4d(base + L::kOffQ + hh * kHalfBytes, &tmQ, q_full, hh * 64, kvh * p.G, q0, b);
-        tma_load_4d(base + L::kOffDO + hh * kHalfBytes, &tmDO, q_full, hh * 64, kvh * p.G, q0, b);
-      }
       bool ok = true;
-      int j = 0;
-      for (; j < n; ++j) {
-        const int s = j % S;
-        ok = mbar_wait(kv_empty(s), ((j / S) & 1) ^ 1, abort_flag, to);
+      int g = 0;                  // K/V tiles loaded so far (ring position)
+      int k = 0;                  // tiles with work so far (Q/dO buffer phase)
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        const Tile T = tile_info(t);
+        if (T.n == 0) continue;
+        // the Q/dO buffer is free once the previous tile's copies into TMEM are done
+        ok = mbar_wait(q_empty, (k & 1) ^ 1, abort_flag, to);
         if (!ok) break;
-        mbar_arrive_expect_tx(kv_full(s), 2u * L::kTileBytes);
+        mbar_arrive_expect_tx(q_full, q_bytes);
         for (int hh = 0; hh < L::kHalves; ++hh) {
-          tma_load_4d(base + L::kOffK + s * L::kTileBytes + hh * kHalfBytes, &tmK, kv_full(s), hh * 64, kvh,
-                      j * kBN, b);
-          tma_load_4d(base + L::kOffV + s * L::kTileBytes + hh * kHalfBytes, &tmV, kv_full(s), hh * 64, kvh,
-                      j * kBN, b);
+          tma_load_4d(base + L::kOffQ + hh * kHalfBytes, &tmQ, q_full, hh * 64, T.kvh * p.G, T.q0, T.b);
+          tma_load_4d(base + L::kOffDO + hh * kHalfBytes, &tmDO, q_full, hh * 64, T.kvh * p.G, T.q0, T.b);
+        }
+        ++k;
+        for (int j = 0; j < T.n; ++j, ++g) {
+          const int s = g % S;
+          ok = mbar_wait(kv_empty(s), ((g / S) & 1) ^ 1, abort_flag, to);
+          if (!ok) break;
+          mbar_arrive_expect_tx(kv_full(s), 2u * L::kTileBytes);
+          for (int hh = 0; hh < L::kHalves; ++hh) {
+            tma_load_4d(base + L::kOffK + s * L::kTileBytes + hh * kHalfBytes, &tmK, kv_full(s), hh * 64,
+                        T.kvh, j * kBN, T.b);
+            tma_load_4d(base + L::kOffV + s * L::kTileBytes + hh * kHalfBytes, &tmV, kv_full(s), hh * 64,
+                        T.kvh, j * kBN, T.b);
+          }
         }
       }
       if (!ok) {
         // let the copies in flight land before the CTA exits: each waited
         // phase belongs to the last load issued into its buffer
         volatile int no_abort = 0;
-        for (int it = j > S ? j - S : 0; it < j; ++it)
+        for (int it = g > S ? g - S : 0; it < g; ++it)
           mbar_wait(kv_full(it % S), (it / S) & 1, &no_abort, 200000000ull);
-        mbar_wait(q_full, 0, &no_abort, 200000000ull);
+        if (k > 0) mbar_wait(q_full, (k - 1) & 1, &no_abort, 200000000ull);
       }
     }
   } else if (warp == kWarpMMA) {
     // ---------------------------------------------------------- MMA issuer
-    if (lane == 0 && n > 0) {
+    if (lane == 0) {
       const uint32_t idesc_s = make_idesc_bf16(128, kBN, 0, 0);   // A in TMEM, B K-major
       const uint32_t idesc_q = make_idesc_bf16(128, D, 0, 1);     // dS in TMEM, K MN-major
-      auto issue_s = [&](int jj) {          // S(jj) = Q K(jj)^T
-        const uint32_t ka = base + L::kOffK + (jj % S) * L::kTileBytes;
+      auto issue_s = [&](int it) {          // S = Q K^T, K from ring stage it % S
+        const uint32_t ka = base + L::kOffK + (it % S) * L::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           umma_ts(tmem + L::kTmS, tmem + L::kTmQ + uint32_t(ks) * 8u, desc_kmajor(ka, ks), idesc_s,
                   ks > 0 ? 1u : 0u);
       };
-      auto issue_dp = [&](int jj) {         // dP(jj) = dO V(jj)^T
-        const uint32_t va = base + L::kOffV + (jj % S) * L::kTileBytes;
+      auto issue_dp = [&](int it) {         // dP = dO V^T
+        const uint32_t va = base + L::kOffV + (it % S) * L::kTileBytes;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
           umma_ts(tmem + L::kTmP, tmem + L::kTmDO + uint32_t(ks) * 8u, desc_kmajor(va, ks), idesc_s,
                   ks > 0 ? 1u : 0u);
       };
-      bool ok = mbar_wait(q_full, 0, abort_flag, to) && mbar_wait(kv_full(0), 0, abort_flag, to);
-      if (ok) {
-        tc_fence_after();
-        copy_tile_to_tmem<D>(tmem + L::kTmQ, base + L::kOffQ);
-        copy_tile_to_tmem<D>(tmem + L::kTmDO, base + L::kOffDO);
-        issue_s(0);
-        issue_dp(0);
-        umma_commit(s_full);
-      }
-      for (int j = 0; ok && j < n; ++j) {
-        const bool more = j + 1 < n;
-        // S(j) and dP(j) have been read: S(j+1) (and dP(j+1)) may overwrite them
-        ok = mbar_wait(sd_read, j & 1, abort_flag, to);
-        if (ok && more) ok = mbar_wait(kv_full((j + 1) % S), ((j + 1) / S) & 1, abort_flag, to);
+      bool ok = true;
+      int g = 0;                  // key-tile iterations so far (all tiles)
+      int k = 0;                  // tiles with work so far
+      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+        const int n = tile_info(t).n;
+        if (n == 0) continue;
+        ok = mbar_wait(q_full, k & 1, abort_flag, to) && mbar_wait(kv_full(g % S), (g / S) & 1, abort_flag, to);
         if (!ok) break;
         tc_fence_after();
-        if (more) {
-          issue_s(j + 1);
+        // executes after every MMA issued before it, so the previous tile's
+        // S and dP products have read the old Q and dO
+        copy_tile_to_tmem<D>(tmem + L::kTmQ, base + L::kOffQ);
+        copy_tile_to_tmem<D>(tmem + L::kTmDO, base + L::kOffDO);
+        umma_commit(q_empty);
+        issue_s(g);
+        issue_dp(g);
+        umma_commit(s_full);
+        for (int j = 0; ok && j < n; ++j) {
+          const int it = g + j;
+          const bool more = j + 1 < n;
+          // S(j) and dP(j) have been read: S(j+1) (and dP(j+1)) may overwrite them
+          ok = mbar_wait(sd_read, it & 1, abort_flag, to);
+          if (ok && more) ok = mbar_wait(kv_full((it + 1) % S), ((it + 1) / S) & 1, abort_flag, to);
+          if (!ok) break;
+          tc_fence_after();
+          if (more) {
+            issue_s(it + 1);
+            if constexpr (L::kSepDS) {
+              issue_dp(it + 1);
+              umma_commit(s_full);
+            }
+          }
+          ok = mbar_wait(p_full, it & 1, abort_flag, to);
+          // the tile's first dQ product overwrites dQ: the previous epilogue must have read it
+          if (ok && j == 0 && k > 0) ok = mbar_wait(dq_free, (k - 1) & 1, abort_flag, to);
+          if (!ok) break;
+          tc_fence_after();
+          // dQ += dS(j) K(j)
+          const uint32_t ka = base + L::kOffK + (it % S) * L::kTileBytes;
+#pragma unroll
+          for (int ks = 0; ks < kBN / 16; ++ks) {
+            const uint32_t acol = L::kSepDS ? L::kTmDS + uint32_t(ks) * 8u : L::kTmP + packed_col(ks);
+            umma_ts(tmem + L::kTmDQ, tmem + acol, desc_mnmajor<D>(ka, ks), idesc_q, (j > 0 || ks > 0) ? 1u : 0u);
+          }
+          umma_commit(kv_empty(it % S));
           if constexpr (L::kSepDS) {
-            issue_dp(j + 1);
+            umma_commit(dq_done);
+          } else if (more) {
+            issue_dp(it + 1);               // dP(j+1) over dS(j), after dQ has read it
             umma_commit(s_full);
           }
         }
-        ok = mbar_wait(p_full, j & 1, abort_flag, to);
         if (!ok) break;
-        tc_fence_after();
-        // dQ += dS(j) K(j)
-        const uint32_t ka = base + L::kOffK + (j % S) * L::kTileBytes;
-#pragma unroll
-        for (int ks = 0; ks < kBN / 16; ++ks) {
-          const uint32_t acol = L::kSepDS ? L::kTmDS + uint32_t(ks) * 8u : L::kTmP + packed_col(ks);
-          umma_ts(tmem + L::kTmDQ, tmem + acol, desc_mnmajor<D>(ka, ks), idesc_q, (j > 0 || ks > 0) ? 1u : 0u);
-        }
-        umma_commit(kv_empty(j % S));
-        if constexpr (L::kSepDS) {
-          umma_commit(dq_done);
-        } else if (more) {
-          issue_dp(j + 1);                  // dP(j+1) over dS(j), after dQ has read it
-          umma_commit(s_full);
-        }
+        umma_commit(done);
+        g += n;
+        ++k;
       }
-      if (ok) umma_commit(done);
       if (!ok) {
         volatile int no_abort = 0;
         umma_commit(drain);
@@ -394,83 +436,108 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int grp = warp >> 2;
     const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
     const int token = r / p.G, gg = r - token * p.G;
-    const int i = q0 + token;
-    const bool row_ok = r < p.G * p.Mq && i < p.Sq;
-    const int h = kvh * p.G + gg;
-    const size_t rowidx = (size_t(b) * p.Hq + h) * p.Sq + i;
-    float lse2 = 0.f, dsum = 0.f;
-    int hi_row = 0;                                     // the row admits keys j < hi_row
-    if (row_ok) {
-      lse2 = p.lse[rowidx] * kLog2e;
-      dsum = p.dsum[rowidx];
-      hi_row = p.causal ? min(Lb, i + diag + 1) : Lb;
-    }
     const uint64_t cl2 = f2_pack(p.scale_log2, p.scale_log2);
-    const uint64_t nl2 = f2_pack(-lse2, -lse2);
-    const uint64_t nd2 = f2_pack(-dsum, -dsum);
     // where this group's dS goes (bf16 pairs, 16 columns)
     const uint32_t ds_col = L::kSepDS ? L::kTmDS + uint32_t(grp) * 16u : L::kTmP + uint32_t(grp) * 32u;
     bool aborted = false;
-    for (int j = 0; j < n; ++j) {
-      bool ok = __all_sync(0xffffffffu, mbar_wait(s_full, j & 1, abort_flag, to));
-      if (!ok) {
-        aborted = true;
-        break;
+    int g = 0;                    // key-tile iterations so far (all tiles)
+    int k = 0;                    // tiles with work so far
+    for (int t = blockIdx.x; !aborted && t < n_tiles; t += gridDim.x) {
+      const Tile T = tile_info(t);
+      const int i = T.q0 + token;
+      const bool row_ok = r < p.G * p.Mq && i < p.Sq;
+      const int h = T.kvh * p.G + gg;
+      __nv_bfloat16* drow = p.dq + ((size_t(T.b) * p.Sq + i) * p.Hq + h) * D + grp * 32;
+      if (T.n == 0) {
+        if (row_ok && grp < D / 32) store_zero_row(drow, 32);    // no admissible key: dQ = 0
+        continue;
       }
-      tc_fence_after();
-      // this warp's 32 keys of the tile: [grp * 32, grp * 32 + 32)
-      const int lim = hi_row - j * kBN - grp * 32;
-      const bool full = __all_sync(0xffffffffu, lim >= 32 || !row_ok);
-      uint32_t sv[32], dp[32], ds[16];
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmS + uint32_t(grp) * 32u, sv);
-      tmem_ld_32x32b_x32(tmem + lane_base + L::kTmP + uint32_t(grp) * 32u, dp);
-      tmem_ld_wait_x32(sv);
-      tmem_ld_wait_x32(dp);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(sd_read);
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        const int k0 = 2 * e;
-        float x0, x1, p0, p1, t0, t1;
-        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[k0]), __uint_as_float(sv[k0 + 1])), cl2, nl2), x0, x1);
-        p0 = ex2_approx(x0);
-        p1 = ex2_approx(x1);
-        if (!full) {
-          p0 = (k0 < lim) ? p0 : 0.f;
-          p1 = (k0 + 1 < lim) ? p1 : 0.f;
-        }
-        f2_unpack(f2_add(f2_pack(__uint_as_float(dp[k0]), __uint_as_float(dp[k0 + 1])), nd2), t0, t1);
-        ds[e] = pack_bf16x2(p0 * t0, p1 * t1);
+      const size_t rowidx = (size_t(T.b) * p.Hq + h) * p.Sq + i;
+      float lse2 = 0.f, dsum = 0.f;
+      int hi_row = 0;                                   // the row admits keys j < hi_row
+      if (row_ok) {
+        lse2 = p.lse[rowidx] * kLog2e;
+        dsum = p.dsum[rowidx];
+        hi_row = p.causal ? min(T.Lb, i + diag + 1) : T.Lb;
       }
-      if (L::kSepDS && j > 0) {
-        // dQ(j-1) must have read dS(j-1) before it is overwritten
-        ok = __all_sync(0xffffffffu, mbar_wait(dq_done, (j - 1) & 1, abort_flag, to));
+      const uint64_t nl2 = f2_pack(-lse2, -lse2);
+      const uint64_t nd2 = f2_pack(-dsum, -dsum);
+      for (int j = 0; j < T.n; ++j) {
+        const int it = g + j;
+        bool ok = __all_sync(0xffffffffu, mbar_wait(s_full, it & 1, abort_flag, to));
         if (!ok) {
           aborted = true;
           break;
         }
         tc_fence_after();
+        // this warp's 32 keys of the tile: [grp * 32, grp * 32 + 32)
+        const int lim = hi_row - j * kBN - grp * 32;
+        const bool full = __all_sync(0xffffffffu, lim >= 32 || !row_ok);
+        // two 16-key chunks through the same registers; S and dP are free for
+        // the next products once the second chunk is in registers
+        uint32_t sv[16], dp[16], ds[16];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          tmem_ld_32x32b_x16(tmem + lane_base + L::kTmS + uint32_t(grp) * 32u + uint32_t(c) * 16u, sv);
+          tmem_ld_32x32b_x16(tmem + lane_base + L::kTmP + uint32_t(grp) * 32u + uint32_t(c) * 16u, dp);
+          tmem_ld_wait_x16(sv);
+          tmem_ld_wait_x16(dp);
+          if (c == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sd_read);
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int k0 = 16 * c + 2 * e;
+            float x0, x1, p0, p1, t0, t1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * e]), __uint_as_float(sv[2 * e + 1])), cl2, nl2), x0,
+                      x1);
+            p0 = ex2_approx(x0);
+            p1 = ex2_approx(x1);
+            if (!full) {
+              p0 = (k0 < lim) ? p0 : 0.f;
+              p1 = (k0 + 1 < lim) ? p1 : 0.f;
+            }
+            f2_unpack(f2_add(f2_pack(__uint_as_float(dp[2 * e]), __uint_as_float(dp[2 * e + 1])), nd2), t0, t1);
+            ds[8 * c + e] = pack_bf16x2(p0 * t0, p1 * t1);
+          }
+        }
+        if (L::kSepDS && it > 0) {
+          // the previous dQ product must have read the dS columns
+          ok = __all_sync(0xffffffffu, mbar_wait(dq_done, (it - 1) & 1, abort_flag, to));
+          if (!ok) {
+            aborted = true;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st_32x32b_x16(tmem + lane_base + ds_col, ds);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
       }
-      tmem_st_32x32b_x16(tmem + lane_base + ds_col, ds);
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    // epilogue: column group grp < D / 32 writes dQ columns [32 grp, 32 grp + 32)
-    __nv_bfloat16* drow = p.dq + ((size_t(b) * p.Sq + i) * p.Hq + h) * D + grp * 32;
-    if (n > 0 && !aborted) {
-      const bool ok = __all_sync(0xffffffffu, mbar_wait(done, 0, abort_flag, to));
+      if (aborted) break;
+      // epilogue: column group grp < D / 32 writes dQ columns [32 grp, 32 grp + 32)
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(done, k & 1, abort_flag, to));
+      if (!ok) {
+        aborted = true;
+        break;
+      }
       tc_fence_after();
-      if (ok && grp < D / 32) {
-        uint32_t v[32];
+      uint32_t v[32];
+      if (grp < D / 32) {
         tmem_ld_32x32b_x32(tmem + lane_base + L::kTmDQ + uint32_t(grp) * 32u, v);
         tmem_ld_wait_x32(v);
-        if (row_ok) store_row32(drow, v, p.scale);
       }
-    } else if (n == 0 && row_ok && grp < D / 32) {
-      store_zero_row(drow, 32);              // no admissible key: dQ = 0
+      // dQ has been read: the next tile's first product may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dq_free);
+      if (row_ok && grp < D / 32) store_row32(drow, v, p.scale);
+      g += T.n;
+      ++k;
     }
   }
 

@@ -277,7 +277,10 @@ int launch_bwd(gqa::bwd::Params p, const void* q, const void* k, const void* v, 
   if (!bwd_smem_attr_set<D>(current_device())) return GQA_ERR_CUDA;
   const long long dsum_threads = (long long)p.B * p.Hq * p.Sq * (D / 8);
   bw::dsum_kernel<D><<<unsigned((dsum_threads + 255) / 256), 256, 0, stream>>>(p);
-  const dim3 gq(unsigned(p.n_qt), unsigned(p.Hkv), unsigned(p.B));
+  // dq_kernel is persistent: at most one CTA per SM, each looping over tiles
+  const long long dq_tiles = (long long)p.n_qt * p.Hkv * p.B;
+  if (dq_tiles > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
+  const unsigned gq = unsigned(std::min<long long>(dq_tiles, num_sms(current_device())));
   bw::dq_kernel<D><<<gq, bw::kThreads, bw::DqLayout<D>::kSmemAlloc, stream>>>(tmQg, tmDOg, tmK, tmV, p);
   const dim3 gk(unsigned(p.n_kt), unsigned(p.Hkv), unsigned(p.B));
   bw::dkdv_kernel<D><<<gk, bw::kThreads, bw::KvLayout<D>::kSmemAlloc, stream>>>(tmK, tmV, tmQ1, tmDO1, p);
