@@ -2,7 +2,7 @@
 // the tcgen05 tensor cores with TMEM accumulators.
 //
 // Sources (page title and section): "FlashAttention Serisi"
-// (webturing.pages.dev), "V2" (a faster backward pass is one of its gains)
+// (webturing.pages.dev), "V2 katkısı" (a faster backward pass is one of its gains)
 // and "Ana fikir" (the softmax intermediates stay out of slow memory; read
 // here as: the weights are rebuilt from the forward's log-sum-exp, nothing
 // quadratic is stored); "3个GQA核心优化技巧" (blog.gitcode.com),

@@ -158,7 +158,7 @@ int gqa_fwd_sparse(const void* q, const void* k, const void* v, void* out, float
 
 /*
  * gqa_bwd -- gradients of gqa_fwd (dense layout) with respect to q, k and v
- * for an upstream gradient dout ([FA-SERIES] "V2" names a faster backward
+ * for an upstream gradient dout ([FA-SERIES] "V2 katkısı" names a faster backward
  * pass as one of its gains, and "Ana fikir" keeps the softmax intermediates
  * out of slow memory; read here as: the weights are rebuilt from the
  * forward's log-sum-exp, never stored.  [GQA-BERT] "GQA的分组共享机制": the
