@@ -189,3 +189,18 @@ def test_bwd_unsupported(lib):
     assert _bwd(lib, dtype=gqa.GQA_DTYPE_FP32) == gqa.GQA_ERR_UNSUPPORTED   # bf16 only
     assert _bwd(lib, D=96) == gqa.GQA_ERR_UNSUPPORTED
     assert _bwd(lib, B=70000) == gqa.GQA_ERR_UNSUPPORTED                   # grid z limit
+
+
+@pytest.mark.parametrize("causal,lens", [(False, None), (True, None), (False, [3, 0, 7]), (True, [5, 2, 7])])
+def test_backward_flops_counts_admissible_pairs(causal, lens):
+    # 10 * D flops per admissible (b, h, i, j), counted here by brute force
+    from grouped_query_attention_08_b300 import roofline
+    B, Hq, Sq, Sk, D = 3, 4, 5, 7, 16
+    pairs = 0
+    for b in range(B):
+        L = Sk if lens is None else lens[b]
+        for i in range(Sq):
+            for j in range(Sk):
+                if j < L and (not causal or j <= i + Sk - Sq):
+                    pairs += Hq
+    assert roofline.backward_flops(B, Hq, Sq, Sk, D, causal, lens) == 10 * D * pairs

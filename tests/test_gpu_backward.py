@@ -119,3 +119,45 @@ def test_bwd_is_deterministic_and_zero_past_the_key_length():
     lens = inp["seqlens_k"].tolist()
     for bi, L in enumerate(lens):
         assert torch.all(a[1][bi, L:] == 0) and torch.all(a[2][bi, L:] == 0)
+
+
+def _full_size(name, seed):
+    """The named workload at full size through the library's forward and
+    backward, as bench.py times it; dO ~ N(0,1) from `seed`."""
+    w = inputs.WORKLOADS[name]
+    inp = inputs.make_workload(w)
+    g = torch.Generator("cpu").manual_seed(seed)
+    dout = torch.randn(tuple(inp["q"].shape), generator=g, dtype=torch.float32).to(torch.bfloat16)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out, lse = gqa.gqa_fwd(d["q"], d["k"], d["v"], causal=w.causal, seqlens_k=d["seqlens_k"], scale=w.scale)
+    dq, dk, dv = gqa.gqa_bwd(d["q"], d["k"], d["v"], out, dout.cuda(), lse, causal=w.causal,
+                             seqlens_k=d["seqlens_k"], scale=w.scale)
+    torch.cuda.synchronize()
+    assert gqa.gqa_device_status() == 0
+    return w, inp, dout, dq.cpu(), dk.cpu(), dv.cpu()
+
+
+def test_bwd_bert_base_full_size_two_batch_entries():
+    # B = 32 launched whole; batch entries 0 and 21 (all their heads) against the oracle
+    w, inp, dout, dq, dk, dv = _full_size("bert_base", 2024)
+    for b in (0, 21):
+        lens = None if inp["seqlens_k"] is None else inp["seqlens_k"][b:b + 1]
+        rq, rk, rv = oracle.attention_backward(inp["q"][b:b + 1], inp["k"][b:b + 1], inp["v"][b:b + 1],
+                                               dout[b:b + 1], scale=w.scale, causal=w.causal, seqlens_k=lens)
+        _cmp(dq[b:b + 1], rq, "dq[b=%d]" % b)
+        _cmp(dk[b:b + 1], rk, "dk[b=%d]" % b)
+        _cmp(dv[b:b + 1], rv, "dv[b=%d]" % b)
+
+
+def test_bwd_bert_large_long_full_size_one_group():
+    # B = 8, S = 4096 launched whole; batch entry 5, K/V head 2 and its G = 6 query heads
+    w, inp, dout, dq, dk, dv = _full_size("bert_large_long", 2025)
+    b, kvh, G = 5, 2, w.Hq // w.Hkv
+    hs = slice(kvh * G, (kvh + 1) * G)
+    sl = lambda t, heads: t[b:b + 1, :, heads]
+    rq, rk, rv = oracle.attention_backward(sl(inp["q"], hs), sl(inp["k"], slice(kvh, kvh + 1)),
+                                           sl(inp["v"], slice(kvh, kvh + 1)), sl(dout, hs), scale=w.scale,
+                                           causal=w.causal)
+    _cmp(sl(dq, hs), rq, "dq")
+    _cmp(sl(dk, slice(kvh, kvh + 1)), rk, "dk")
+    _cmp(sl(dv, slice(kvh, kvh + 1)), rv, "dv")
