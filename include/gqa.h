@@ -181,11 +181,15 @@ int gqa_fwd_sparse(const void* q, const void* k, const void* v, void* out, float
  *                 keys >= L_b get zeros)
  *   scale, causal, seqlens_k  as gqa_fwd (and must be what it was given)
  *   dtype         GQA_DTYPE_BF16 only (GQA_DTYPE_FP32 -> GQA_ERR_UNSUPPORTED)
- * D 64 or 128 (GQA_ERR_UNSUPPORTED otherwise); all bf16 tensors 16-byte
- * aligned; B, Hq <= 65535.  Gradients accumulate in fp32; P and dS are
- * rounded to bf16 for the products.  No atomics: the result does not depend
- * on scheduling.  Buffers must not overlap.  Launches three kernels on
- * `stream` and returns without synchronising.
+ * D 64 or 128, G = Hq/Hkv <= 128, B and Hq <= 65535 (GQA_ERR_UNSUPPORTED
+ * otherwise); all bf16 tensors 16-byte aligned, lse and dsum 4-byte aligned
+ * (GQA_ERR_INVALID_ARG otherwise, as for a NULL pointer, Hq % Hkv != 0, a
+ * non-finite scale or causal not 0/1).  A key length outside [0, Sk] raises
+ * GQA_ERR_DEVICE_BOUNDS in gqa_device_status() and counts as 0; a wait that
+ * gives up raises GQA_ERR_DEVICE_TIMEOUT.  Gradients accumulate in fp32; P
+ * and dS are rounded to bf16 for the products.  No atomics: the result does
+ * not depend on scheduling.  Buffers must not overlap.  Launches three
+ * kernels on `stream` and returns without synchronising.
  */
 int gqa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
             const float* lse, float* dsum, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,

@@ -204,3 +204,7 @@ def test_backward_flops_counts_admissible_pairs(causal, lens):
                 if j < L and (not causal or j <= i + Sk - Sq):
                     pairs += Hq
     assert roofline.backward_flops(B, Hq, Sq, Sk, D, causal, lens) == 10 * D * pairs
+
+
+def test_bwd_rejects_groups_wider_than_a_tile(lib):
+    assert _bwd(lib, Hq=130, Hkv=1) == gqa.GQA_ERR_UNSUPPORTED    # 128 rows hold one token of each head
