@@ -2,10 +2,10 @@
 // the tcgen05 tensor cores with TMEM accumulators.
 //
 // Sources (page title and section): "FlashAttention Serisi"
-// (webturing.pages.dev), "V2 katkısı" (a faster backward pass is one of its gains)
-// and "Ana fikir" (the softmax intermediates stay out of slow memory; read
-// here as: the weights are rebuilt from the forward's log-sum-exp, nothing
-// quadratic is stored); "3个GQA核心优化技巧" (blog.gitcode.com),
+// (webturing.pages.dev), "V2 katkısı" (a faster backward pass is one of its
+// gains) and "Ana fikir" (the softmax intermediates stay out of slow memory;
+// read here as: the weights are rebuilt from the forward's log-sum-exp,
+// nothing quadratic is stored); "3个GQA核心优化技巧" (blog.gitcode.com),
 // "GQA的分组共享机制": the G query heads of a group share one K/V head, so
 // that head's gradient is the sum over the group.
 //
@@ -16,23 +16,24 @@
 //   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_{h in group, i} dS_ij q_i
 // Three kernels, no atomics, so the result does not depend on scheduling:
 //  * dsum_kernel: Dsum per query row.
-//  * dq_kernel, one CTA per (b, kvh, Mq tokens x G heads = one 128-row tile,
-//    row = token * G + head-in-group, as in the forward): per 128-key tile
-//    S = Q K^T and dP = dO V^T into TMEM, dS = P (dP - Dsum) written back
-//    over S as packed bf16, dQ += dS K accumulated in TMEM.
+//  * dq_kernel, persistent (one CTA per SM looping over tiles), a tile being
+//    Mq tokens x G heads of K/V head kvh = 128 rows (row = token * G +
+//    head-in-group, as in the forward): per 128-key tile S = Q K^T and
+//    dP = dO V^T into TMEM, dS = P (dP - Dsum) written back as packed bf16,
+//    dQ += dS K accumulated in TMEM.
 //  * dkdv_kernel, one CTA per (b, kvh, 128 keys): for every head of the group
 //    and every query tile of 128, S^T = K Q^T and dP^T = V dO^T into TMEM,
-//    P^T and dS^T written back over them, dV += P^T dO and dK += dS^T Q
+//    P^T and dS^T written back over dP^T, dV += P^T dO and dK += dS^T Q
 //    accumulated in TMEM over the whole loop (the group sum).
 // Warp roles (576 threads): warps 0-15 the elementwise step and the
 // epilogue, one TMEM lane (tile row) per thread and warp w taking the 32
 // columns of group w / 4 of the row (four warps per SM sub-partition, so
 // TMEM-load and MUFU latencies overlap), warp 16 TMA producer, warp 17 MMA
-// issuer.  Tiles arrive by TMA with the 128-byte swizzle; operands that stay
-// fixed for the whole CTA (Q and dO in dq_kernel) are copied into TMEM with
-// tcgen05.cp and read from there as the A operand, which leaves the
-// shared-memory operand bandwidth to the streamed tiles.  All waits are bounded: on a timeout the kernel raises a device
-// error, drains its copies and MMAs, and exits.
+// issuer.  Tiles arrive by TMA with the 128-byte swizzle; the dq_kernel
+// tile's Q and dO are copied into TMEM with tcgen05.cp and read from there
+// as the A operand, which leaves the shared-memory operand bandwidth to the
+// streamed K/V tiles.  All waits are bounded: on a timeout the kernel raises
+// a device error, drains its copies and MMAs, and exits.
 #pragma once
 
 #include "common.cuh"
