@@ -25,6 +25,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -85,7 +86,8 @@ class ClockSampler:
     def __init__(self, device_index):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", "clocks_bench_%d.csv" % os.getpid())
+        # raw samples (the JSON line carries their summary)
+        self.path = os.path.join(tempfile.gettempdir(), "gqa_bench_clocks_%d.csv" % os.getpid())
 
     def __enter__(self):
         try:
