@@ -146,6 +146,12 @@ def _barrier(ws):
         dist.barrier()
 
 
+def _whole_job_rate(work_per_step, steps, ws, seconds):
+    """Work all ranks did per second: every rank (replica) does `work_per_step`
+    per step, and `seconds` is the slowest rank's time for `steps` steps."""
+    return work_per_step * steps * ws / seconds
+
+
 def _max_over_ranks(x, ws, device):
     if ws == 1:
         return x
@@ -488,8 +494,8 @@ def main():
     dec_s = _max_over_ranks(sum(t_dec) / 1e3, ws, device)
     total_s = _max_over_ranks(total_ms / 1e3, ws, device)
 
-    value = flops_p * K * ws / pre_s / 1e12
-    dec_gbs = kv_bytes_d * K * ws / dec_s / 1e9
+    value = _whole_job_rate(flops_p, K, ws, pre_s) / 1e12
+    dec_gbs = _whole_job_rate(kv_bytes_d, K, ws, dec_s) / 1e9
     peaks, psrc = _peaks()
     pre_avg = pre_s / K
     dec_avg = dec_s / K
@@ -542,7 +548,7 @@ def main():
         b.record()
         torch.cuda.synchronize()
         e2e_s = _max_over_ranks(a.elapsed_time(b) / 1e3, ws, device)
-        e2e = {"value": flops_p * args.e2e_steps * ws / e2e_s / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": _whole_job_rate(flops_p, args.e2e_steps, ws, e2e_s) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "what": "prefill through gqa_fwd with pinned host inputs copied in and out every step"}
 
