@@ -122,6 +122,13 @@ def _stream(device, stream=None):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _expect(t, shape, dtype, name):
+    """A caller-provided buffer must have exactly the shape and dtype the
+    library writes (the C ABI sees only a pointer)."""
+    if t is not None and (tuple(t.shape) != tuple(shape) or t.dtype != dtype):
+        raise ValueError("%s must be %s %s, got %s %s" % (name, dtype, list(shape), t.dtype, list(t.shape)))
+
+
 def _check_cuda(*ts):
     dev = None
     for t in ts:
@@ -157,6 +164,8 @@ def gqa_fwd(q, k, v, *, causal=False, seqlens_k=None, scale=None, out=None, lse=
     code = _dtype_code(q)
     if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or tuple(seqlens_k.shape) != (B,)):
         raise ValueError("seqlens_k must be int32 [B]")
+    _expect(out, q.shape, q.dtype, "out")
+    _expect(lse, (B, Hq, Sq), torch.float32, "lse")
     if out is None:
         out = torch.empty_like(q)
     if lse is None and return_lse:
@@ -201,6 +210,8 @@ def gqa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q=None, ma
         max_seqlen_q = int((cu_seqlens_q[1:] - cu_seqlens_q[:-1]).max().item())
     if max_seqlen_k is None:
         max_seqlen_k = int((cu_seqlens_k[1:] - cu_seqlens_k[:-1]).max().item())
+    _expect(out, q.shape, q.dtype, "out")
+    _expect(lse, (Hq, total_q), torch.float32, "lse")
     if out is None:
         out = torch.empty_like(q)
     if lse is None and return_lse:
@@ -240,6 +251,8 @@ def gqa_fwd_sparse(q, k, v, block_mask, block_size, *, causal=False, seqlens_k=N
         raise ValueError("block_mask must be uint8 [ceil(Sq/bs), ceil(Sk/bs)]")
     if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or tuple(seqlens_k.shape) != (B,)):
         raise ValueError("seqlens_k must be int32 [B]")
+    _expect(out, q.shape, q.dtype, "out")
+    _expect(lse, (B, Hq, Sq), torch.float32, "lse")
     if out is None:
         out = torch.empty_like(q)
     if lse is None and return_lse:
@@ -276,6 +289,10 @@ def gqa_bwd(q, k, v, out, dout, lse, *, causal=False, seqlens_k=None, scale=None
         raise ValueError("lse must be float32 [B, Hq, Sq]")
     if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or tuple(seqlens_k.shape) != (B,)):
         raise ValueError("seqlens_k must be int32 [B]")
+    _expect(dq, q.shape, torch.bfloat16, "dq")
+    _expect(dk, k.shape, torch.bfloat16, "dk")
+    _expect(dv, k.shape, torch.bfloat16, "dv")
+    _expect(dsum, (B, Hq, Sq), torch.float32, "dsum")
     if dq is None:
         dq = torch.empty_like(q)
     if dk is None:
@@ -325,6 +342,7 @@ def gqa_decode(q, kcache, vcache, cache_seqlens, *, scale=None, num_splits=0, ou
     code = _dtype_code(q)
     if cache_seqlens.dtype != torch.int32 or tuple(cache_seqlens.shape) != (B,):
         raise ValueError("cache_seqlens must be int32 [B]")
+    _expect(out, q.shape, q.dtype, "out")
     if out is None:
         out = torch.empty_like(q)
     need = gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, Smax)
@@ -363,6 +381,7 @@ def gqa_decode_fp8(q, kcache, vcache, cache_seqlens, k_scale, v_scale, *, scale=
             raise TypeError("the caches must be float8_e4m3fn (or uint8 e4m3 bytes)")
     if cache_seqlens.dtype != torch.int32 or tuple(cache_seqlens.shape) != (B,):
         raise ValueError("cache_seqlens must be int32 [B]")
+    _expect(out, q.shape, q.dtype, "out")
     if out is None:
         out = torch.empty_like(q)
     need = gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, Smax)
@@ -399,9 +418,18 @@ def gqa_decode_noalloc(q, kcache, vcache, cache_seqlens, *, scale=None, num_spli
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     fn.restype = i32
     fn.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, f32, i32, i32, i32, vp]
+    if q.dim() != 3 or kcache.dim() != 4 or vcache.dim() != 4:
+        raise ValueError("q must be [B,Hq,D] and caches [B,Smax,Hkv,D]")
     B, Hq, D = q.shape
-    _, Smax, Hkv, _ = kcache.shape
+    Bk, Smax, Hkv, Dk = kcache.shape
+    if Bk != B or Dk != D or tuple(vcache.shape) != tuple(kcache.shape):
+        raise ValueError("shape mismatch between q and the caches")
+    if q.dtype != kcache.dtype or q.dtype != vcache.dtype:
+        raise TypeError("q and the caches must share a dtype")
+    if cache_seqlens.dtype != torch.int32 or tuple(cache_seqlens.shape) != (B,):
+        raise ValueError("cache_seqlens must be int32 [B]")
     code = _dtype_code(q)
+    _expect(out, q.shape, q.dtype, "out")
     if out is None:
         out = torch.empty_like(q)
     dev = _check_cuda(q, kcache, vcache, cache_seqlens, out)
