@@ -263,3 +263,41 @@ def attention_backward(q, k, v, dout, *, scale=None, causal=False, seqlens_k=Non
             dk[b, :, g, :] += scale * (ds.T @ q[b, :, h, :])
             dv[b, :, g, :] += p.T @ do[b, :, h, :]
     return dq, dk, dv
+
+
+def attention_backward_dq_rows(q, k, v, dout, rows, *, scale=None, causal=False, seqlens_k=None):
+    """dQ of `attention_backward` for selected query rows only, each computed on
+    its own from the definition (the row's exact softmax P_i over its
+    admissible keys, dP_i = dO_i V^T, Dsum_i = P_i . dP_i, dQ_i = scale
+    (P_i * (dP_i - Dsum_i)) K): for checks at sizes where the full gradient is
+    too large for the CPU.  rows: (b, h, i) triples.  Returns [len(rows), D]
+    float64.
+    """
+    B, Sq, Hq, D = q.shape
+    Sk, Hkv = k.shape[1], k.shape[2]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    lens = None if seqlens_k is None else np.asarray(
+        seqlens_k.cpu().numpy() if hasattr(seqlens_k, "cpu") else seqlens_k).astype(np.int64)
+    out = np.zeros((len(rows), D), np.float64)
+    for n, (b, h, i) in enumerate(rows):
+        g = h // G
+        kb = _f32(k[b, :, g, :]).astype(np.float64)
+        vb = _f32(v[b, :, g, :]).astype(np.float64)
+        qi = _f32(q[b, i, h, :]).astype(np.float64)
+        doi = _f32(dout[b, i, h, :]).astype(np.float64)
+        j = np.arange(Sk)
+        allowed = j < (Sk if lens is None else lens[b])
+        if causal:
+            allowed &= j <= i + Sk - Sq
+        if not allowed.any():
+            continue
+        s = scale * (kb @ qi)
+        m = s[allowed].max()
+        w = np.where(allowed, np.exp(np.where(allowed, s, m) - m), 0.0)
+        p = w / w.sum()
+        dp = vb @ doi
+        dsum = float((p * dp).sum())
+        out[n] = scale * ((p * (dp - dsum)) @ kb)
+    return out

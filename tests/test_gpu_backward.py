@@ -161,3 +161,18 @@ def test_bwd_bert_large_long_full_size_one_group():
     _cmp(sl(dq, hs), rq, "dq")
     _cmp(sl(dk, slice(kvh, kvh + 1)), rk, "dk")
     _cmp(sl(dv, slice(kvh, kvh + 1)), rv, "dv")
+
+
+def test_bwd_causal_long_full_size_sampled_dq_rows():
+    # B = 4, Hq = 32, S = 8192, D = 128, causal, launched whole; 48 sampled
+    # (b, h, i) rows of dQ, among them the first and last query rows, each
+    # computed on its own by the oracle
+    w, inp, dout, dq, dk, dv = _full_size("causal_long", 2026)
+    rng = np.random.default_rng(7)
+    rows = [(0, 0, 0), (w.B - 1, w.Hq - 1, w.Sq - 1), (1, 5, 1), (2, 17, w.Sq // 2)]
+    rows += [(int(rng.integers(w.B)), int(rng.integers(w.Hq)), int(rng.integers(w.Sq))) for _ in range(44)]
+    ref = oracle.attention_backward_dq_rows(inp["q"], inp["k"], inp["v"], dout, rows, scale=w.scale,
+                                            causal=w.causal)
+    got = torch.stack([dq[b, i, h] for b, h, i in rows])
+    _cmp(got, ref, "dq rows")
+    assert torch.isfinite(dk.float()).all() and torch.isfinite(dv.float()).all()

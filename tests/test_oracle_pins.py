@@ -578,3 +578,18 @@ def test_backward_oracle_matches_central_differences():
             xm[idx] -= eps
             fd = (loss_with(which, xp) - loss_with(which, xm)) / (2 * eps)
             assert abs(fd - g[idx]) <= 2e-4 * max(1.0, abs(g[idx])), (idx, fd, g[idx])
+
+
+@pytest.mark.parametrize("causal,lens,G", [(False, None, 4), (True, None, 2), (True, [6, 0], 3), (False, [9, 3], 1)])
+def test_backward_dq_rows_are_the_full_oracle_rows(causal, lens, G):
+    # the row-by-row dQ (for checks at full size) against the full oracle gradient
+    rng = np.random.default_rng(21 + G)
+    B, Sq, Sk, Hkv, D = 2, 7, 9, 2, 8
+    Hq = Hkv * G
+    q, k, v = _rand((B, Sq, Hq, D), rng), _rand((B, Sk, Hkv, D), rng), _rand((B, Sk, Hkv, D), rng)
+    do = _rand((B, Sq, Hq, D), rng)
+    dq, _, _ = oracle.attention_backward(q, k, v, do, scale=0.3, causal=causal, seqlens_k=lens)
+    rows = [(b, h, i) for b in range(B) for h in range(Hq) for i in range(Sq)]
+    got = oracle.attention_backward_dq_rows(q, k, v, do, rows, scale=0.3, causal=causal, seqlens_k=lens)
+    ref = np.stack([dq[b, i, h] for b, h, i in rows])
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
