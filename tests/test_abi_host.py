@@ -208,3 +208,16 @@ def test_backward_flops_counts_admissible_pairs(causal, lens):
 
 def test_bwd_rejects_groups_wider_than_a_tile(lib):
     assert _bwd(lib, Hq=130, Hkv=1) == gqa.GQA_ERR_UNSUPPORTED    # 128 rows hold one token of each head
+
+
+def test_product_code_does_not_touch_the_oracle():
+    # the oracle is test infrastructure: nothing in the package (binding,
+    # build script, inputs, roofline, CUDA sources) imports, loads or names it
+    import pathlib
+    pkg = pathlib.Path(gqa.__file__).parent
+    files = [p for p in pkg.rglob("*") if p.suffix in (".py", ".cu", ".cuh", ".h", ".c")]
+    assert files
+    for p in files:
+        text = p.read_text()
+        assert "import oracle" not in text and "from oracle" not in text, p
+        assert "liboracle" not in text and "oracle/" not in text, p
