@@ -41,14 +41,14 @@ METRIC = "GQA prefill TFLOP/s & decode KV-cache GB/s on 1 B300, % of roofline"
 PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 
 # DRAM traffic per launch from one ncu capture, valid only while the kernel
-# source is unchanged (sha256 of the file below).  Filled from the committed
-# profiles/*.md summaries; None = not captured for the current source.
+# source is unchanged (sha256 of the file below); None = not captured for the
+# current source.
 NCU_TRAFFIC = {
-    # profiles/prefill_kernel_d64_bert_base.md (one launch, bert_base)
+    # one launch on bert_base
     "prefill": {"source": "grouped_query_attention_08_b300/csrc/prefill_sm103.cuh",
                 "sha256": "597407912e03c9d5f670a6fef6109fe8531859762cf0fdef7c02f64bd8cd5c42",
                 "workload": "bert_base", "bytes": 95083776},
-    # profiles/decode_split_kernel_llama_decode_small.md (B=16 capture scaled to B=64 by KV bytes)
+    # a B=16 capture scaled to B=64 by valid KV bytes
     "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh",
                "sha256": "bdbf5370ee5f9909a3c8113f1991ca09478653442bedf0c446fbd2db9b8c7ef8",
                "workload": "llama_decode", "bytes": 1275700000},
@@ -398,6 +398,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4000)
     ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--warmup-seconds", type=float, default=1.5,
+                    help="minimum wall time of back-to-back warm-up steps right before the timed steps")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--prefill", default="bert_base",
                     choices=["bert_base", "bert_large_long", "causal_long"])
@@ -459,18 +461,34 @@ def main():
         gqa.gqa_decode(Dd["q"], Dd["kcache"], Dd["vcache"], Dd["cache_seqlens"], scale=wd.scale,
                        num_splits=0, out=out_d, workspace=work)
 
-    for _ in range(args.warmup):
-        flush.fill_(1)
+    def step(i):
+        flush.fill_(i & 0xFF)
         prefill()
         decode()
+
+    # one untimed step checks that the path runs cleanly before anything else
+    step(1)
     torch.cuda.synchronize()
     if gqa.gqa_device_status() != 0:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError("device error in the first step")
 
     K = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
+        # Warm-up inside the clock sampler and right before the timed steps:
+        # at least W steps and at least --warmup-seconds of back-to-back work,
+        # so that a short timed region starts on a GPU already in its
+        # steady state (no idle gap, clocks up, caches and TLBs warm).
+        t0 = time.perf_counter()
+        n_warm = 0
+        while n_warm < args.warmup or time.perf_counter() - t0 < args.warmup_seconds:
+            for _ in range(8):
+                step(n_warm)
+                n_warm += 1
+            torch.cuda.synchronize()
+        if gqa.gqa_device_status() != 0:
+            raise RuntimeError("device error during warm-up")
         _barrier(ws)
         torch.cuda.synchronize()
         t_start.record()
@@ -493,6 +511,13 @@ def main():
     pre_s = _max_over_ranks(sum(t_pre) / 1e3, ws, device)
     dec_s = _max_over_ranks(sum(t_dec) / 1e3, ws, device)
     total_s = _max_over_ranks(total_ms / 1e3, ws, device)
+
+    # per-step distribution (this rank): median and min beside the mean
+    per_step = {"prefill_ms": {"mean": statistics.fmean(t_pre), "median": statistics.median(t_pre),
+                               "min": min(t_pre), "max": max(t_pre)},
+                "decode_ms": {"mean": statistics.fmean(t_dec), "median": statistics.median(t_dec),
+                              "min": min(t_dec), "max": max(t_dec)},
+                "warmup_steps_run": n_warm, "timed_region_ms": total_ms}
 
     value = _whole_job_rate(flops_p, K, ws, pre_s) / 1e12
     dec_gbs = _whole_job_rate(kv_bytes_d, K, ws, dec_s) / 1e9
@@ -591,7 +616,10 @@ def main():
                     wd.name, wd.B, wd.Hq, wd.Hkv, wd.D, wd.Smax, wd.lens[0], wd.lens[1])),
                 "l2": "256 MB L2 flush before every step; decode inputs (2.1 GB caches) exceed L2",
                 "parallelism": "replicas" if ws > 1 else "single GPU",
-                "prefill_ms": pre_avg * 1e3, "decode_ms": dec_avg * 1e3, "decode_num_splits": nsplit},
+                "prefill_ms": pre_avg * 1e3, "decode_ms": dec_avg * 1e3, "decode_num_splits": nsplit,
+                "warmup": "%d steps and >= %.1f s of back-to-back steps inside the clock sampler, "
+                          "immediately before the timed steps" % (args.warmup, args.warmup_seconds)},
+            "per_step": per_step,
             "roofline": roof_p,
             "decode": {"value": dec_gbs, "unit": "GB/s (KV-cache bytes read / decode time)",
                        "roofline": roof_d, "kv_bytes_per_step": kv_bytes_d},

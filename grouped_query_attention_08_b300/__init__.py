@@ -34,6 +34,8 @@ GQA_ERR_DEVICE_TIMEOUT = 4
 GQA_ERR_DEVICE_BOUNDS = 5
 GQA_DTYPE_BF16 = 0
 GQA_DTYPE_FP32 = 1
+# size of gqa_decode_noalloc's library-owned scratch (GQA_DECODE_NOALLOC_SCRATCH_BYTES in gqa.h)
+GQA_DECODE_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libgqa.so")
@@ -145,6 +147,12 @@ def _check_cuda(*ts):
     return dev
 
 
+def _on(dev):
+    """Makes the tensors' device current for a library call: libgqa reads the
+    current device for its per-device state and the stream's device."""
+    return _torch().cuda.device(dev)
+
+
 def gqa_fwd(q, k, v, *, causal=False, seqlens_k=None, scale=None, out=None, lse=None,
             return_lse=True, stream=None):
     """Prefill / encoder GQA attention.  q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D] (bf16 or fp32, CUDA).
@@ -173,9 +181,10 @@ def gqa_fwd(q, k, v, *, causal=False, seqlens_k=None, scale=None, out=None, lse=
     dev = _check_cuda(q, k, v, out, lse, seqlens_k)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    rc = load_library().gqa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
-                                float(scale), int(bool(causal)), _ptr(seqlens_k), code,
-                                _stream(dev, stream))
+    with _on(dev):
+        rc = load_library().gqa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                                    float(scale), int(bool(causal)), _ptr(seqlens_k), code,
+                                    _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_fwd")
     return out, lse
@@ -219,10 +228,11 @@ def gqa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, *, max_seqlen_q=None, ma
     dev = _check_cuda(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    rc = load_library().gqa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
-                                       _ptr(cu_seqlens_k), B, Hq, Hkv, max(int(max_seqlen_q), 1),
-                                       max(int(max_seqlen_k), 1), total_q, total_k, D, float(scale),
-                                       int(bool(causal)), code, _stream(dev, stream))
+    with _on(dev):
+        rc = load_library().gqa_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                                           _ptr(cu_seqlens_k), B, Hq, Hkv, max(int(max_seqlen_q), 1),
+                                           max(int(max_seqlen_k), 1), total_q, total_k, D, float(scale),
+                                           int(bool(causal)), code, _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_fwd_varlen")
     return out, lse
@@ -260,9 +270,10 @@ def gqa_fwd_sparse(q, k, v, block_mask, block_size, *, causal=False, seqlens_k=N
     dev = _check_cuda(q, k, v, out, lse, seqlens_k, block_mask)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    rc = load_library().gqa_fwd_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(block_mask), bs,
-                                       B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)), _ptr(seqlens_k),
-                                       code, _stream(dev, stream))
+    with _on(dev):
+        rc = load_library().gqa_fwd_sparse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(block_mask), bs,
+                                           B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)), _ptr(seqlens_k),
+                                           code, _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_fwd_sparse")
     return out, lse
@@ -304,9 +315,10 @@ def gqa_bwd(q, k, v, out, dout, lse, *, causal=False, seqlens_k=None, scale=None
     dev = _check_cuda(q, k, v, out, dout, lse, dsum, dq, dk, dv, seqlens_k)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    rc = load_library().gqa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dsum), _ptr(dq),
-                                _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)),
-                                _ptr(seqlens_k), GQA_DTYPE_BF16, _stream(dev, stream))
+    with _on(dev):
+        rc = load_library().gqa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dsum), _ptr(dq),
+                                    _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, D, float(scale), int(bool(causal)),
+                                    _ptr(seqlens_k), GQA_DTYPE_BF16, _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_bwd")
     return dq, dk, dv
@@ -352,9 +364,10 @@ def gqa_decode(q, kcache, vcache, cache_seqlens, *, scale=None, num_splits=0, ou
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load_library().gqa_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_seqlens), _ptr(out),
-                                   B, Hq, Hkv, D, float(scale), int(num_splits), Smax, code,
-                                   _ptr(workspace), wbytes, _stream(dev, stream))
+    with _on(dev):
+        rc = load_library().gqa_decode(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_seqlens), _ptr(out),
+                                       B, Hq, Hkv, D, float(scale), int(num_splits), Smax, code,
+                                       _ptr(workspace), wbytes, _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_decode")
     return out
@@ -391,9 +404,10 @@ def gqa_decode_fp8(q, kcache, vcache, cache_seqlens, k_scale, v_scale, *, scale=
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     wbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    rc = load_library().gqa_decode_fp8(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_seqlens), _ptr(out),
-                                       B, Hq, Hkv, D, float(scale), float(k_scale), float(v_scale),
-                                       int(num_splits), Smax, _ptr(workspace), wbytes, _stream(dev, stream))
+    with _on(dev):
+        rc = load_library().gqa_decode_fp8(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_seqlens), _ptr(out),
+                                           B, Hq, Hkv, D, float(scale), float(k_scale), float(v_scale),
+                                           int(num_splits), Smax, _ptr(workspace), wbytes, _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_decode_fp8")
     return out
@@ -435,8 +449,9 @@ def gqa_decode_noalloc(q, kcache, vcache, cache_seqlens, *, scale=None, num_spli
     dev = _check_cuda(q, kcache, vcache, cache_seqlens, out)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    rc = fn(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_seqlens), _ptr(out), B, Hq, Hkv, D, float(scale),
-            int(num_splits), Smax, code, _stream(dev, stream))
+    with _on(dev):
+        rc = fn(_ptr(q), _ptr(kcache), _ptr(vcache), _ptr(cache_seqlens), _ptr(out), B, Hq, Hkv, D, float(scale),
+                int(num_splits), Smax, code, _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_decode_noalloc")
     return out

@@ -67,6 +67,10 @@ struct Params {
   float scale;
   float scale_log2;             // scale * log2(e)
   unsigned long long timeout_ns;
+  // Test hook: when nonzero, the MMA issuer of dq_kernel and dkdv_kernel first
+  // waits on its abort barrier, which nothing arrives on yet, so the wait runs
+  // out after timeout_ns and the CTA takes its abort path.
+  int test_stall;
 };
 
 // Key length of batch entry b (a bad length raises a device error and
@@ -367,7 +371,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ts(tmem + L::kTmP, tmem + L::kTmDO + uint32_t(ks) * 8u, desc_kmajor(va, ks), idesc_s,
                   ks > 0 ? 1u : 0u);
       };
-      bool ok = true;
+      // test hook: `drain` has no arrival yet
+      bool ok = !p.test_stall || mbar_wait(drain, 0, abort_flag, to);
       int g = 0;                  // key-tile iterations so far (all tiles)
       int k = 0;                  // tiles with work so far
       for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
@@ -683,7 +688,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_ss(tmem + tm_dp(t), desc_kmajor(base + L::kOffV, ks), desc_kmajor(da, ks), idesc_s,
                   ks > 0 ? 1u : 0u);
       };
-      bool ok = mbar_wait(kv_full, 0, abort_flag, to) && mbar_wait(qd_full(0), 0, abort_flag, to);
+      // test hook: `drain` has no arrival yet
+      bool ok = !p.test_stall || mbar_wait(drain, 0, abort_flag, to);
+      ok = ok && mbar_wait(kv_full, 0, abort_flag, to) && mbar_wait(qd_full(0), 0, abort_flag, to);
       if (ok) {
         tc_fence_after();
         issue_st(0);

@@ -46,13 +46,21 @@ int current_device() {
   return d;
 }
 
+// Limit of every bounded pipeline wait inside the kernels: 2 s, or the value
+// of the environment variable GQA_WAIT_TIMEOUT_NS (nanoseconds), read at each
+// launch so that a process can shorten it for one call and restore it.
 unsigned long long wait_timeout_ns() {
-  static unsigned long long v = [] {
-    const char* e = std::getenv("GQA_WAIT_TIMEOUT_NS");
-    unsigned long long t = e ? std::strtoull(e, nullptr, 10) : 0ull;
-    return t > 0 ? t : 2000000000ull;   // 2 s
-  }();
-  return v;
+  const char* e = std::getenv("GQA_WAIT_TIMEOUT_NS");
+  const unsigned long long t = e ? std::strtoull(e, nullptr, 10) : 0ull;
+  return t > 0 ? t : 2000000000ull;
+}
+
+// Test hook: a nonzero GQA_TEST_FORCE_TIMEOUT makes the next launches of the
+// prefill and backward kernels wait on a barrier nothing arrives on, so that
+// their bounded waits run out and the abort paths run (read at each launch).
+int force_timeout() {
+  const char* e = std::getenv("GQA_TEST_FORCE_TIMEOUT");
+  return (e && e[0] && e[0] != '0') ? 1 : 0;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -192,6 +200,7 @@ int launch_prefill_bf16(const void* q, const void* k, const void* v, void* out, 
   p.causal = causal ? 1 : 0;
   p.scale_log2 = scale * kLog2e;
   p.timeout_ns = wait_timeout_ns();
+  p.test_stall = force_timeout();
   if (bmask)
     pf::prefill_kernel<D, false, true><<<unsigned(grid), pf::kThreads, pf::Layout<D>::kSmemAlloc, stream>>>(
         tmQ, tmK, tmV, tmO, p);
@@ -263,6 +272,7 @@ int launch_bwd(gqa::bwd::Params p, const void* q, const void* k, const void* v, 
   p.n_kt = (p.Sk + bw::kBN - 1) / bw::kBN;
   p.scale_log2 = p.scale * kLog2e;
   p.timeout_ns = wait_timeout_ns();
+  p.test_stall = force_timeout();
   // dq_kernel: Q / dO tiles of Mq tokens x G heads (row = token * G + head),
   // K / V tiles of 128 keys; dkdv_kernel: Q / dO tiles of 128 tokens of one
   // head, K / V tiles of 128 keys.
@@ -733,7 +743,9 @@ int gqa_device_status(void* stream) {
 // split partials live in a fixed scratch array that belongs to the library.
 namespace {
 
-constexpr size_t kStaticScratchBytes = size_t(32) << 20;   // 32 MiB per device
+// The size is the one gqa.h publishes (32 MiB per device).
+constexpr size_t kStaticScratchBytes = size_t(GQA_DECODE_NOALLOC_SCRATCH_BYTES);
+static_assert(kStaticScratchBytes == (size_t(32) << 20), "the header documents a 32 MiB scratch");
 
 // File-scope device array: every device that loads this library holds one
 // copy until the process exits.  In host code the name is only a stand-in

@@ -148,6 +148,11 @@ struct Params {
   int causal;
   float scale_log2;       // scale * log2(e)
   unsigned long long timeout_ns;
+  // Test hook: when nonzero, Q tile 0's MMA issuer first waits on a barrier
+  // that nothing arrives on, so the wait runs out after timeout_ns and the
+  // whole CTA takes its abort path (device timeout status, drained copies
+  // and MMAs, TMEM freed).
+  int test_stall;
 };
 
 struct Unit {
@@ -590,7 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t g = 0;           // key tiles of earlier units (K/V ring position; s_full / p_full phases)
       uint32_t qn = 0;          // units with work so far
       uint32_t n2 = 0;          // units with two or more key tiles so far (s_free / pv_done phases)
-      bool ok = true;
+      // test hook: `drain` (tile 0's abort barrier) has no arrival yet
+      bool ok = !(p.test_stall && tq == 0) || mbar_wait(drain, 0, abort_flag, to);
       for (uint32_t k = 0; ok; ++k) {
         SeqInfo sq;
         const int u = next_unit(k, sq, ok, false);

@@ -41,12 +41,25 @@
  *   - dtype: GQA_DTYPE_BF16 (q/k/v/out bfloat16, fp32 accumulation,
  *     tcgen05 tensor cores) or GQA_DTYPE_FP32 (q/k/v/out float32, exact
  *     fp32 SIMT check path).  lse is always float32.
- *   - stream is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *   - stream is a cudaStream_t (NULL = legacy default stream) of the
+ *     CURRENT device, and every pointer lives on that device: the library
+ *     reads the current device for its per-device state (SM count, kernel
+ *     attributes, work-unit scheduler slots, scratch addresses).  Calls only
  *     enqueue work: they never synchronise, so errors found on the device
  *     (a key length out of range, a pipeline wait that timed out) are
  *     reported later by gqa_device_status().
  *   - Return value: a gqa_status code.  On any non-OK return nothing has
  *     been enqueued.
+ *   - Bounded waits: every pipeline wait inside the prefill and backward
+ *     kernels gives up after GQA_WAIT_TIMEOUT_NS nanoseconds (environment
+ *     variable, default 2e9, read at each call); the CTA then drains its
+ *     copies and matrix products, frees its tensor memory and exits, and the
+ *     call reports GQA_ERR_DEVICE_TIMEOUT through gqa_device_status().
+ *     Until that status has been read (which clears it), later launches on
+ *     the device give up at their first wait that does not complete at once.
+ *     A nonzero GQA_TEST_FORCE_TIMEOUT (read at each call) is a test hook:
+ *     one MMA-issuing thread per CTA first waits on a barrier nothing
+ *     arrives on, so that the abort path runs.
  */
 #ifndef GQA_H_
 #define GQA_H_
@@ -66,6 +79,8 @@ typedef enum {
     GQA_ERR_DEVICE_BOUNDS = 5    /* a device-side length check failed (reported by gqa_device_status) */
 } gqa_status;
 
+/* Arithmetic path of a call.  The names carry a DTYPE_ infix (GQA_DTYPE_BF16
+ * rather than GQA_BF16) so that they cannot be mistaken for status codes. */
 typedef enum {
     GQA_DTYPE_BF16 = 0,
     GQA_DTYPE_FP32 = 1
@@ -213,7 +228,10 @@ int gqa_decode_num_splits(int B, int Hkv, int max_seqlen_k, int num_splits);
  * gqa_decode_workspace_bytes -- device scratch gqa_decode needs for the
  * split partials: fp32 O_s [B, Hq, n, D] plus fp32 lse_s [B, Hq, n], where
  * n = gqa_decode_num_splits(B, Hkv, max_seqlen_k, num_splits).  Returns 0
- * when n == 1 (no combine step) and 0 for invalid arguments.
+ * when n == 1 (no combine step) and 0 for invalid arguments.  Hkv is an
+ * argument because the automatic split count (num_splits <= 0) depends on
+ * the number of (batch, K/V head) pairs the split kernel runs over.  No page
+ * defines this call: it sizes the caller-owned workspace of the split step.
  */
 size_t gqa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits,
                                   int max_seqlen_k);
@@ -310,11 +328,14 @@ int gqa_decode_noalloc(const void* q, const void* kcache, const void* vcache,
  * gqa_device_status -- synchronises `stream`, then returns and clears the
  * library's device error word for the current device: GQA_OK,
  * GQA_ERR_DEVICE_BOUNDS or GQA_ERR_DEVICE_TIMEOUT (GQA_ERR_CUDA if the
- * synchronisation itself failed).
+ * synchronisation itself failed).  The stream's device must be the current
+ * device.  No page defines this call: it reports the device-side checks of
+ * the kernels (key lengths, bounded pipeline waits).
  */
 int gqa_device_status(void* stream);
 
-/* gqa_status_string -- static, human-readable name of a status code. */
+/* gqa_status_string -- static, human-readable name of a status code.  No
+ * page defines this call. */
 const char* gqa_status_string(int status);
 
 #ifdef __cplusplus

@@ -86,7 +86,18 @@ def _sample(w, n, seed, extra=()):
     return inputs.sample_rows(total, n, seed, must=must).numpy()
 
 
-@pytest.mark.parametrize("name", ["bert_base", "bert_large_long", "causal_long"])
+def test_bert_base_workload_every_row():
+    """The headline workload at full size, every one of its B * Hq * Sq =
+    393,216 output rows against the oracle (a few seconds of oracle time)."""
+    w = inputs.WORKLOADS["bert_base"]
+    inp = inputs.make_workload(w)
+    out, lse = _run(to_dev(inp), w.scale, w.causal)
+    ref_o, ref_l = oracle_fwd(inp, w.scale, w.causal)
+    compare(out.float().cpu().numpy(), ref_o, torch.bfloat16, what="bert_base")
+    compare_lse(lse.cpu().numpy(), ref_l, torch.bfloat16)
+
+
+@pytest.mark.parametrize("name", ["bert_large_long", "causal_long"])
 def test_full_workloads_on_sampled_rows(name):
     w = inputs.WORKLOADS[name]
     inp = inputs.make_workload(w)

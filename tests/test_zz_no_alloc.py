@@ -15,9 +15,8 @@ import torch
 
 import grouped_query_attention_08_b300 as gqa
 from grouped_query_attention_08_b300 import build, inputs
-from parity import compare
 
-SCRATCH = 32 << 20
+SCRATCH = gqa.GQA_DECODE_NOALLOC_SCRATCH_BYTES
 
 
 def _lib():
@@ -54,7 +53,6 @@ def test_rejects_calls_beyond_the_scratch_size():
 def test_noalloc_decode_matches_gqa_decode_on_two_calls_in_a_row(dtype):
     lib = _lib()
     code = gqa.GQA_DTYPE_BF16 if dtype == "bf16" else gqa.GQA_DTYPE_FP32
-    tdt = torch.bfloat16 if dtype == "bf16" else torch.float32
     for call, seed in enumerate((21, 22)):       # different inputs: stale scratch contents cannot pass
         inp = inputs.make_decode(16, 64, 8, 128, 4096, seed=seed, lens=(1, 4096), dtype=dtype)
         d = {k: v.cuda() for k, v in inp.items()}
@@ -66,4 +64,6 @@ def test_noalloc_decode_matches_gqa_decode_on_two_calls_in_a_row(dtype):
         assert rc == gqa.GQA_OK, gqa.gqa_status_string(rc)
         torch.cuda.synchronize()
         assert gqa.gqa_device_status() == 0
-        compare(out.float().cpu().numpy(), ref.float().cpu().numpy(), tdt, what="noalloc call %d" % call)
+        # the same kernels on the same inputs, so the outputs agree bit for bit
+        # (a scratch corrupted by an earlier call cannot hide inside a tolerance)
+        assert torch.equal(out, ref), "noalloc call %d differs from gqa_decode" % call
