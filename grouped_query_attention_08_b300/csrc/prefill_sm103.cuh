@@ -226,16 +226,28 @@ DEVI uint64_t tiles_of_blocks(int bs, uint64_t lo, uint64_t hi, int half) {
   return even_bits(a) | (even_bits(b) << 32);
 }
 
-// Position of work unit u = qidx * (B * Hkv) + b * Hkv + kvh.
+// Position of work unit u.  Non-causal: u = qidx * (B * Hkv) + b * Hkv + kvh,
+// so the units running at one time spread over every (b, kvh) and their
+// lengths even out.  Causal: u = (b * Hkv + kvh) * n_qblk + qidx, so the
+// units running at one time are Q blocks of the same one or two (b, kvh):
+// they read the same K/V tiles, which then come from L2 instead of DRAM
+// (a long causal launch holds far more K/V than L2 does); qidx counts the
+// Q blocks longest first (unit_info), which keeps the tail short.
 struct UnitPos {
   int u, qidx, b, kvh;
 };
 DEVI UnitPos upos_of(const Params& p, int u) {
   UnitPos x;
   x.u = u;
-  const int bh_count = p.B * p.Hkv;
-  x.qidx = u / bh_count;
-  const int bh = u - x.qidx * bh_count;
+  int bh;
+  if (p.causal) {
+    bh = u / p.n_qblk;
+    x.qidx = u - bh * p.n_qblk;
+  } else {
+    const int bh_count = p.B * p.Hkv;
+    x.qidx = u / bh_count;
+    bh = u - x.qidx * bh_count;
+  }
   x.b = bh / p.Hkv;
   x.kvh = bh - x.b * p.Hkv;
   return x;
