@@ -142,6 +142,29 @@ __global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const Params
   const int kend = min(Lb, kstart + p.split_len);
   const int nblk = kend > kstart ? (kend - kstart + kBlockKeys - 1) / kBlockKeys : 0;
 
+  const size_t row_stride = size_t(p.Hkv) * D;                       // bytes
+  const uint8_t* kbase = p.kc + (size_t(b) * p.Smax * p.Hkv + kvh) * D;
+  const uint8_t* vbase = p.vc + (size_t(b) * p.Smax * p.Hkv + kvh) * D;
+
+  float o[MT][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;   // heads 2c and 2c+1
+
+  // The ring prologue goes out before q is loaded and scaled, so the first
+  // blocks' memory latency overlaps q's.
+  using RG = RingF8;
+  extern __shared__ __align__(16) uint8_t dsmem[];
+  const uint32_t ring = smem_u32(dsmem) + uint32_t(warp) * RG::kWarpBytes;
+#pragma unroll
+  for (int i = 0; i < RG::kRing - 1; ++i) {
+    const int bi = warp + i * kWarps;
+    if (bi < nblk)
+      issue_block_f8(ring + uint32_t(i) * RG::kSlotBytes, kbase, vbase, row_stride, kstart + bi * kBlockKeys, kend,
+                     kstart, lane);
+    else
+      cp_async_commit();
+  }
   // Q^T fragments (head n = r; zero if n >= G), dims d0..d0+3 of k-step ks
   // with d0 = 16 (c + 4 (ks / 4)) + 4 (ks % 4) -- the order in which the K
   // chunks below deliver them.  The whole group is scaled by 2^e so that its
@@ -179,27 +202,6 @@ __global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const Params
   }
   const float cl = p.scale_k_log2 * ldexpf(1.f, -ex);
 
-  const size_t row_stride = size_t(p.Hkv) * D;                       // bytes
-  const uint8_t* kbase = p.kc + (size_t(b) * p.Smax * p.Hkv + kvh) * D;
-  const uint8_t* vbase = p.vc + (size_t(b) * p.Smax * p.Hkv + kvh) * D;
-
-  float o[MT][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
-  float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;   // heads 2c and 2c+1
-
-  using RG = RingF8;
-  extern __shared__ __align__(16) uint8_t dsmem[];
-  const uint32_t ring = smem_u32(dsmem) + uint32_t(warp) * RG::kWarpBytes;
-#pragma unroll
-  for (int i = 0; i < RG::kRing - 1; ++i) {
-    const int bi = warp + i * kWarps;
-    if (bi < nblk)
-      issue_block_f8(ring + uint32_t(i) * RG::kSlotBytes, kbase, vbase, row_stride, kstart + bi * kBlockKeys, kend,
-                     kstart, lane);
-    else
-      cp_async_commit();
-  }
   BlockF8 cur;
   int it = 0;
   for (int blk = warp; blk < nblk; blk += kWarps, ++it) {
