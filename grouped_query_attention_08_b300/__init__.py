@@ -9,6 +9,7 @@ raise.
 
 Functions keep the C names:
   gqa_fwd(q, k, v, *, causal=False, seqlens_k=None, scale=None, out=None, lse=None, return_lse=True)
+  gqa_fwd_host(q, k, v, *, causal=False, seqlens_k=None, scale=None, ..., staging=None, chunk_b=0)
   gqa_decode(q, kcache, vcache, cache_seqlens, *, scale=None, num_splits=0, out=None, workspace=None)
   gqa_fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *, causal=False, ...)
   gqa_fwd_sparse(q, k, v, block_mask, block_size, *, causal=False, seqlens_k=None, ...)
@@ -66,6 +67,9 @@ def load_library():
         vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.gqa_fwd.restype = i32
         lib.gqa_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, i32, vp]
+        lib.gqa_fwd_host.restype = i32
+        lib.gqa_fwd_host.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp, i32, vp, vp, vp,
+                                     vp, vp, vp, i32, vp]
         lib.gqa_fwd_varlen.restype = i32
         lib.gqa_fwd_varlen.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32,
                                        f32, i32, i32, vp]
@@ -187,6 +191,63 @@ def gqa_fwd(q, k, v, *, causal=False, seqlens_k=None, scale=None, out=None, lse=
                                     _stream(dev, stream))
     if rc != GQA_OK:
         raise GQAError(rc, "gqa_fwd")
+    return out, lse
+
+
+def gqa_fwd_host(q, k, v, *, causal=False, seqlens_k=None, scale=None, out=None, lse=None, return_lse=True,
+                 staging=None, chunk_b=0, device=None, stream=None):
+    """gqa_fwd for host-resident tensors: q [B,Sq,Hq,D], k/v [B,Sk,Hkv,D] CPU tensors (bf16 or
+    fp32; page-locked for the copies to overlap), optional int32 CPU seqlens_k [B].  The batch
+    is cut into chunks whose copies in, attention and copies out overlap on three streams.
+
+    Returns (out, lse) CPU tensors (allocated page-locked when not given).  The call only
+    enqueues work: the outputs are complete once the stream has completed
+    (torch.cuda.current_stream(device).synchronize()).  ``staging`` is an optional dict of
+    device tensors ``q, k, v, out, lse, seqlens`` of the full sizes, reused across calls;
+    missing ones are allocated on ``device`` (default: the current CUDA device).
+    """
+    torch = _torch()
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be 4-D [B, S, H, D]")
+    B, Sq, Hq, D = q.shape
+    Bk, Sk, Hkv, Dk = k.shape
+    if Bk != B or Dk != D or tuple(v.shape) != tuple(k.shape):
+        raise ValueError("shape mismatch between q, k and v")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise TypeError("q, k, v must share a dtype")
+    code = _dtype_code(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("seqlens_k", seqlens_k), ("out", out), ("lse", lse)):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("%s must be a contiguous CPU tensor" % name)
+    if seqlens_k is not None and (seqlens_k.dtype != torch.int32 or tuple(seqlens_k.shape) != (B,)):
+        raise ValueError("seqlens_k must be int32 [B]")
+    _expect(out, q.shape, q.dtype, "out")
+    _expect(lse, (B, Hq, Sq), torch.float32, "lse")
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    if lse is None and return_lse:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32).pin_memory()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    st = {} if staging is None else staging
+    need = {"q": (q.shape, q.dtype), "k": (k.shape, k.dtype), "v": (v.shape, v.dtype), "out": (q.shape, q.dtype)}
+    if lse is not None:
+        need["lse"] = ((B, Hq, Sq), torch.float32)
+    if seqlens_k is not None:
+        need["seqlens"] = ((B,), torch.int32)
+    for name, (shape, dtype) in need.items():
+        if st.get(name) is None:
+            st[name] = torch.empty(tuple(shape), dtype=dtype, device=dev)
+        _expect(st[name], shape, dtype, "staging[%r]" % name)
+    _check_cuda(*[st[n] for n in need])
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with _on(dev):
+        rc = load_library().gqa_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, Sq, Sk, D,
+                                         float(scale), int(bool(causal)), _ptr(seqlens_k), code, _ptr(st["q"]),
+                                         _ptr(st["k"]), _ptr(st["v"]), _ptr(st["out"]), _ptr(st.get("lse")),
+                                         _ptr(st.get("seqlens")), int(chunk_b), _stream(dev, stream))
+    if rc != GQA_OK:
+        raise GQAError(rc, "gqa_fwd_host")
     return out, lse
 
 

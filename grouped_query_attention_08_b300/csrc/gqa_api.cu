@@ -356,28 +356,50 @@ const char* gqa_status_string(int status) {
   }
 }
 
-int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv, int Sq,
-            int Sk, int D, float scale, int causal, const int* seqlens_k, int dtype, void* stream) {
+}  // extern "C"
+
+namespace {
+
+// Argument checks of gqa_fwd: GQA_OK when the call would launch its kernel.
+int fwd_arg_status(const void* q, const void* k, const void* v, const void* out, const float* lse, int B, int Hq,
+                   int Hkv, int Sq, int Sk, int D, float scale, int causal, const int* seqlens_k, int dtype) {
   if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return GQA_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return GQA_ERR_INVALID_ARG;
   if (!q || !k || !v || !out) return GQA_ERR_INVALID_ARG;
   if (!std::isfinite(scale)) return GQA_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return GQA_ERR_INVALID_ARG;
   if ((lse && !aligned(lse, 4)) || (seqlens_k && !aligned(seqlens_k, 4))) return GQA_ERR_INVALID_ARG;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (dtype == GQA_DTYPE_BF16) {
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return GQA_ERR_INVALID_ARG;
     if (D != 64 && D != 128) return GQA_ERR_UNSUPPORTED;
     if (Hq / Hkv > gqa::prefill::kBM) return GQA_ERR_UNSUPPORTED;
     if ((long long)Hq * D * Sq * B > (1LL << 40)) return GQA_ERR_UNSUPPORTED;
+    return GQA_OK;
+  }
+  if (dtype == GQA_DTYPE_FP32) {
+    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4)) return GQA_ERR_INVALID_ARG;
+    if (D > gqa::f32::kMaxD) return GQA_ERR_UNSUPPORTED;
+    return GQA_OK;
+  }
+  return GQA_ERR_INVALID_ARG;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int Hq, int Hkv, int Sq,
+            int Sk, int D, float scale, int causal, const int* seqlens_k, int dtype, void* stream) {
+  const int arg = fwd_arg_status(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, D, scale, causal, seqlens_k, dtype);
+  if (arg != GQA_OK) return arg;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (dtype == GQA_DTYPE_BF16) {
     return D == 64 ? launch_prefill_bf16<64>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k,
                                              nullptr, nullptr, 0, 0, nullptr, 0, st)
                    : launch_prefill_bf16<128>(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, scale, causal, seqlens_k,
                                               nullptr, nullptr, 0, 0, nullptr, 0, st);
   }
-  if (dtype == GQA_DTYPE_FP32) {
-    if (!aligned(q, 4) || !aligned(k, 4) || !aligned(v, 4) || !aligned(out, 4)) return GQA_ERR_INVALID_ARG;
-    if (D > gqa::f32::kMaxD) return GQA_ERR_UNSUPPORTED;
+  {
     gqa::f32::Params p{};
     p.q = static_cast<const float*>(q);
     p.k = static_cast<const float*>(k);
@@ -405,7 +427,112 @@ int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse, 
     p.len_cap = Sk;
     return launch_f32(p, st);
   }
-  return GQA_ERR_INVALID_ARG;
+}
+
+}  // extern "C"
+
+// ===================================================== host-buffer prefill
+// Copy streams and events of gqa_fwd_host, created once per device.
+namespace {
+
+constexpr int kHostPipeMaxChunks = 64;
+
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t in_done[kHostPipeMaxChunks] = {};
+  cudaEvent_t comp_done[kHostPipeMaxChunks] = {};
+};
+
+std::mutex g_host_pipe_mu;
+HostPipe g_host_pipe[kMaxDevices];
+
+HostPipe* host_pipe(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_host_pipe_mu);
+  HostPipe& hp = g_host_pipe[dev];
+  if (!hp.ready) {
+    const unsigned ev = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.start, ev) == cudaSuccess &&
+              cudaEventCreateWithFlags(&hp.done, ev) == cudaSuccess;
+    for (int i = 0; ok && i < kHostPipeMaxChunks; ++i)
+      ok = cudaEventCreateWithFlags(&hp.in_done[i], ev) == cudaSuccess &&
+           cudaEventCreateWithFlags(&hp.comp_done[i], ev) == cudaSuccess;
+    if (!ok) return nullptr;
+    hp.ready = true;
+  }
+  return &hp;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gqa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* out_h, float* lse_h, int B, int Hq,
+                 int Hkv, int Sq, int Sk, int D, float scale, int causal, const int* seqlens_k_h, int dtype,
+                 void* q_d, void* k_d, void* v_d, void* out_d, float* lse_d, int* seqlens_d, int chunk_b,
+                 void* stream) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || D <= 0) return GQA_ERR_INVALID_ARG;
+  if (!q_h || !k_h || !v_h || !out_h || !q_d || !k_d || !v_d || !out_d) return GQA_ERR_INVALID_ARG;
+  if ((lse_h == nullptr) != (lse_d == nullptr)) return GQA_ERR_INVALID_ARG;
+  if ((seqlens_k_h == nullptr) != (seqlens_d == nullptr)) return GQA_ERR_INVALID_ARG;
+  // the whole call's arguments, as gqa_fwd checks them, before anything is
+  // enqueued (every chunk then passes the same checks)
+  const int arg = fwd_arg_status(q_d, k_d, v_d, out_d, lse_d, B, Hq, Hkv, Sq, Sk, D, scale, causal, seqlens_d, dtype);
+  if (arg != GQA_OK) return arg;
+  const size_t esz = dtype == GQA_DTYPE_BF16 ? 2 : 4;
+  int cb = chunk_b > 0 ? chunk_b : std::max(1, B / 8);
+  cb = std::max(cb, (B + kHostPipeMaxChunks - 1) / kHostPipeMaxChunks);   // at most kHostPipeMaxChunks chunks
+  cb = std::min(cb, B);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  HostPipe* hp = host_pipe(current_device());
+  if (!hp) return GQA_ERR_CUDA;
+  // per batch entry
+  const size_t qb = size_t(Sq) * Hq * D * esz, kb = size_t(Sk) * Hkv * D * esz, lb = size_t(Hq) * Sq * 4;
+  auto c8 = [](const void* p, size_t off) { return static_cast<const char*>(p) + off; };
+  auto m8 = [](void* p, size_t off) { return static_cast<char*>(p) + off; };
+  // the copy streams start after the work already enqueued on `stream`
+  if (cudaEventRecord(hp->start, st) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  int rc = GQA_OK;
+  int ci = 0;
+  for (int b0 = 0; b0 < B; b0 += cb, ++ci) {
+    const int nb = std::min(cb, B - b0);
+    // inputs of the chunk: host -> device
+    if (cudaMemcpyAsync(m8(q_d, b0 * qb), c8(q_h, b0 * qb), nb * qb, cudaMemcpyHostToDevice, hp->in) != cudaSuccess ||
+        cudaMemcpyAsync(m8(k_d, b0 * kb), c8(k_h, b0 * kb), nb * kb, cudaMemcpyHostToDevice, hp->in) != cudaSuccess ||
+        cudaMemcpyAsync(m8(v_d, b0 * kb), c8(v_h, b0 * kb), nb * kb, cudaMemcpyHostToDevice, hp->in) != cudaSuccess ||
+        (seqlens_d && cudaMemcpyAsync(seqlens_d + b0, seqlens_k_h + b0, nb * sizeof(int), cudaMemcpyHostToDevice,
+                                      hp->in) != cudaSuccess) ||
+        cudaEventRecord(hp->in_done[ci], hp->in) != cudaSuccess ||
+        cudaStreamWaitEvent(st, hp->in_done[ci], 0) != cudaSuccess) {
+      rc = GQA_ERR_CUDA;
+      break;
+    }
+    // the chunk's attention on `stream`
+    rc = gqa_fwd(c8(q_d, b0 * qb), c8(k_d, b0 * kb), c8(v_d, b0 * kb), m8(out_d, b0 * qb),
+                 lse_d ? reinterpret_cast<float*>(m8(lse_d, b0 * lb)) : nullptr, nb, Hq, Hkv, Sq, Sk, D, scale, causal,
+                 seqlens_d ? seqlens_d + b0 : nullptr, dtype, stream);
+    if (rc != GQA_OK) break;
+    // outputs of the chunk: device -> host
+    if (cudaEventRecord(hp->comp_done[ci], st) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->out, hp->comp_done[ci], 0) != cudaSuccess ||
+        cudaMemcpyAsync(m8(out_h, b0 * qb), c8(out_d, b0 * qb), nb * qb, cudaMemcpyDeviceToHost, hp->out) !=
+            cudaSuccess ||
+        (lse_d && cudaMemcpyAsync(m8(lse_h, b0 * lb), c8(lse_d, b0 * lb), nb * lb, cudaMemcpyDeviceToHost, hp->out) !=
+                      cudaSuccess)) {
+      rc = GQA_ERR_CUDA;
+      break;
+    }
+  }
+  // `stream` completes only after the last copy (also after a failure part-way)
+  if (cudaEventRecord(hp->done, hp->out) != cudaSuccess || cudaStreamWaitEvent(st, hp->done, 0) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  return rc;
 }
 
 int gqa_fwd_varlen(const void* q, const void* k, const void* v, void* out, float* lse, const int* cu_seqlens_q,

@@ -117,6 +117,45 @@ int gqa_fwd(const void* q, const void* k, const void* v, void* out, float* lse,
             const int* seqlens_k, int dtype, void* stream);
 
 /*
+ * gqa_fwd_host -- gqa_fwd for inputs and outputs that live in host memory:
+ * the batch is cut into chunks of batch entries, and each chunk's inputs go
+ * host -> device, its attention runs, and its outputs go device -> host, on
+ * three streams so that the two copy directions and the computation of
+ * different chunks overlap.  The computation is exactly gqa_fwd's (one
+ * gqa_fwd launch per chunk on `stream`; the outputs equal gqa_fwd's bit for
+ * bit).  [GQA-BERT] "阶段二" (a batch of encoder sequences); no page defines
+ * the copy pipeline, which only moves the data the method reads and writes.
+ *
+ *   q_h, k_h, v_h     host, read; layouts as gqa_fwd.  For the copies to run
+ *                     asynchronously and overlap, host buffers must be
+ *                     page-locked (cudaHostAlloc / cudaHostRegister);
+ *                     pageable memory still gives correct results, with
+ *                     copies that do not overlap.
+ *   out_h             host, written, [B, Sq, Hq, D]
+ *   lse_h             host, written, [B, Hq, Sq] fp32; may be NULL
+ *   seqlens_k_h       host int32 [B] or NULL, as gqa_fwd's seqlens_k
+ *   q_d, k_d, v_d, out_d   device buffers of the full tensors' sizes, owned
+ *                     by the caller (staging; the library allocates nothing)
+ *   lse_d             device [B, Hq, Sq] fp32, or NULL when lse_h is NULL
+ *   seqlens_d         device int32 [B], or NULL when seqlens_k_h is NULL
+ *   chunk_b           batch entries per chunk; <= 0 = automatic (B / 8,
+ *                     at least 1)
+ *   other arguments   as gqa_fwd
+ * The call returns after enqueueing; the host outputs are complete once
+ * `stream` has completed (the library makes `stream` wait for its copy
+ * streams).  The host input buffers must not change, and the host output
+ * buffers must not be read, before that.  The copy streams and events are
+ * created once per device, on the first call with that device current.
+ * Each chunk is one gqa_fwd launch and counts towards gqa_fwd's limit of 64
+ * launches in flight per device.
+ * Returns GQA_OK, GQA_ERR_INVALID_ARG, GQA_ERR_UNSUPPORTED or GQA_ERR_CUDA.
+ */
+int gqa_fwd_host(const void* q_h, const void* k_h, const void* v_h, void* out_h, float* lse_h,
+                 int B, int Hq, int Hkv, int Sq, int Sk, int D, float scale, int causal,
+                 const int* seqlens_k_h, int dtype, void* q_d, void* k_d, void* v_d, void* out_d,
+                 float* lse_d, int* seqlens_d, int chunk_b, void* stream);
+
+/*
  * gqa_fwd_varlen -- gqa_fwd over sequences of different lengths packed
  * back to back without padding (the BERT batching case: [GQA-BERT]
  * "阶段二" passes padding_mask / seqlen_k for sequences of unequal length;

@@ -78,6 +78,36 @@ def test_fwd_fp32_head_dim_limit(lib):
     assert _fwd(lib, D=257, dtype=1) == gqa.GQA_ERR_UNSUPPORTED
 
 
+def _fwd_host(lib, B=2, Hq=4, Hkv=2, Sq=8, Sk=8, D=64, scale=0.125, causal=0, dtype=0, qh=FAKE, oh=FAKE,
+              lse_h=None, lse_d=None, sl_h=None, sl_d=None, qd=FAKE, chunk_b=0):
+    P = ctypes.c_void_p
+    opt = lambda x: P(x) if x else None  # noqa: E731
+    return lib.gqa_fwd_host(P(qh), P(FAKE), P(FAKE), P(oh), opt(lse_h), B, Hq, Hkv, Sq, Sk, D, scale, causal,
+                            opt(sl_h), dtype, P(qd), P(FAKE), P(FAKE), P(FAKE), opt(lse_d), opt(sl_d), chunk_b, None)
+
+
+@pytest.mark.parametrize("kw", [dict(B=0), dict(Hq=6, Hkv=4), dict(qh=0), dict(oh=0), dict(qd=0),
+                                dict(lse_h=FAKE), dict(lse_d=FAKE), dict(sl_h=FAKE), dict(sl_d=FAKE),
+                                dict(qd=FAKE + 8), dict(scale=float("nan")), dict(causal=3), dict(dtype=5)])
+def test_fwd_host_rejects_invalid_arguments_before_any_copy(lib, kw):
+    # every rejection happens before a copy is enqueued (fake pointers are never touched)
+    assert _fwd_host(lib, **kw) == gqa.GQA_ERR_INVALID_ARG
+
+
+def test_fwd_host_unsupported_head_dim(lib):
+    assert _fwd_host(lib, D=96) == gqa.GQA_ERR_UNSUPPORTED
+
+
+def test_fwd_host_binding_refuses_device_tensors():
+    import torch
+    q = torch.zeros((1, 4, 4, 64), dtype=torch.bfloat16)
+    k = torch.zeros((1, 4, 2, 64), dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        gqa.gqa_fwd_host(q, k, k.clone(), seqlens_k=torch.zeros((2,), dtype=torch.int32))
+    with pytest.raises(ValueError):
+        gqa.gqa_fwd_host(q, k[:, :, :1], k)
+
+
 def _fwd_varlen(lib, B=2, Hq=4, Hkv=2, msq=8, msk=8, tq=12, tk=12, D=64, scale=0.125, causal=0, dtype=0,
                 q=FAKE, k=FAKE, v=FAKE, out=FAKE, lse=None, cuq=FAKE, cuk=FAKE):
     P = ctypes.c_void_p
