@@ -97,6 +97,34 @@ DEVI void issue_block_f8(uint32_t slot, const uint8_t* kbase, const uint8_t* vba
   cp_async_commit();
 }
 
+// Per-lane copy offsets of a 16-key block, fixed for the whole kernel: copy i
+// of a lane moves 16-byte chunk (lane % 8) of row (lane / 8) + 4 (i % 4) of K
+// (i < 4) or V (i >= 4).  goff: byte offset of that source chunk from the
+// block's first cached row; soff: its swizzled place in the ring slot.
+struct F8Copy {
+  uint32_t goff[4];
+  uint32_t soff[8];
+};
+DEVI F8Copy f8_copy_offsets(size_t row_stride, int lane) {
+  F8Copy cp;
+  const int chunk = lane & 7;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) cp.goff[j] = uint32_t(((lane >> 3) + 4 * j) * row_stride) + 16u * uint32_t(chunk);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int row = (i < 4 ? 0 : kBlockKeys) + (lane >> 3) + 4 * (i & 3);
+    cp.soff[i] = uint32_t(row) * RingF8::kRowBytes + (uint32_t(chunk) ^ swz(row)) * 16u;
+  }
+  return cp;
+}
+// A block whose 16 keys are all valid: every copy moves 16 bytes.
+DEVI void issue_full_block_f8(uint32_t slot, const uint8_t* kblk, const uint8_t* vblk, const F8Copy& cp) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    cp_async_16(slot + cp.soff[i], (i < 4 ? kblk : vblk) + cp.goff[i & 3], 16u);
+  cp_async_commit();
+}
+
 // Raw e4m3 fragments of a block: K rows (r, r+8) chunks (c, c+4); V rows
 // (2c, 2c+1, 2c+8, 2c+9) chunk r.
 struct BlockF8 {
@@ -156,12 +184,20 @@ __global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const Params
   using RG = RingF8;
   extern __shared__ __align__(16) uint8_t dsmem[];
   const uint32_t ring = smem_u32(dsmem) + uint32_t(warp) * RG::kWarpBytes;
+  const F8Copy cpo = f8_copy_offsets(row_stride, lane);
+  // a block of 16 valid keys takes the precomputed copy offsets; the
+  // sequence's last, partial block zero-fills its keys past the end
+  auto issue = [&](uint32_t slot, int k0) {
+    if (k0 + kBlockKeys <= kend)
+      issue_full_block_f8(slot, kbase + size_t(k0) * row_stride, vbase + size_t(k0) * row_stride, cpo);
+    else
+      issue_block_f8(slot, kbase, vbase, row_stride, k0, kend, kstart, lane);
+  };
 #pragma unroll
   for (int i = 0; i < RG::kRing - 1; ++i) {
     const int bi = warp + i * kWarps;
     if (bi < nblk)
-      issue_block_f8(ring + uint32_t(i) * RG::kSlotBytes, kbase, vbase, row_stride, kstart + bi * kBlockKeys, kend,
-                     kstart, lane);
+      issue(ring + uint32_t(i) * RG::kSlotBytes, kstart + bi * kBlockKeys);
     else
       cp_async_commit();
   }
@@ -213,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const Params
       const int nb = blk + (RG::kRing - 1) * kWarps;
       const uint32_t slot = ring + uint32_t((it + RG::kRing - 1) % RG::kRing) * RG::kSlotBytes;
       if (nb < nblk)
-        issue_block_f8(slot, kbase, vbase, row_stride, kstart + nb * kBlockKeys, kend, kstart, lane);
+        issue(slot, kstart + nb * kBlockKeys);
       else
         cp_async_commit();
     }
