@@ -717,16 +717,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool aborted = false;
 
     const int r_tok = r / p.G;   // token of this row within the Q tile
+    // The next unit's queue entry is read one unit ahead, while the current
+    // unit's last PV runs (before its epilogue can read O).
+    SeqInfo sq_next;
+    bool next_ok;
+    int u_next = next_unit(0, sq_next, next_ok, true);
+    next_ok = __all_sync(0xffffffffu, next_ok);
     for (uint32_t k = 0; !aborted; ++k) {
-      SeqInfo sq;
-      bool qok;
-      const int u = next_unit(k, sq, qok, true);
-      if (!__all_sync(0xffffffffu, qok)) {
+      if (!next_ok) {
         aborted = true;
         break;
       }
-      if (u >= p.n_units) break;
-      const Unit U = unit_info<kPacked, kSparse>(p, upos_of(p, u), sq);
+      if (u_next >= p.n_units) break;
+      const Unit U = unit_info<kPacked, kSparse>(p, upos_of(p, u_next), sq_next);
       const int token = U.q0 + t * p.Mq + r_tok;
       const bool row_ok = (r < rows_per_tile) && (token < U.Lq);
       int limit = 0;
@@ -910,6 +913,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(p_full(t));
       }
 
+      if (!aborted) {
+        u_next = next_unit(k + 1, sq_next, next_ok, true);
+        next_ok = __all_sync(0xffffffffu, next_ok);
+      }
+
       // ---------------------------------------------------------- epilogue
       bool have_o = (U.n_tiles > 0) && !aborted;
       if (have_o) {
@@ -997,7 +1005,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!aborted && row_ok && p.lse) {
-        const float lse = (l > 0.f && have_o) ? (m + log2f(l)) * 0.6931471805599453f : -INFINITY;
+        float lg;
+        asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(l));
+        const float lse = (l > 0.f && have_o) ? (m + lg) * 0.6931471805599453f : -INFINITY;
         p.lse[(size_t(U.tb) * p.Hq + size_t(U.kvh) * p.G + g) * size_t(p.lse_stride) + size_t(U.qbase) + token] =
             lse;
       }
