@@ -46,8 +46,8 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # one launch on bert_base
     "prefill": {"source": "grouped_query_attention_08_b300/csrc/prefill_sm103.cuh",
-                "sha256": "261cb75df8b2a0b4c2ed8c3859cfe527b2370090a861710530497185257ed22f",
-                "workload": "bert_base", "bytes": 95807744},
+                "sha256": "5cc4f8841ac12ade15ed0f9f1520581132fd7ef85d5156ddb8f96d0cedc888e9",
+                "workload": "bert_base", "bytes": 94322432},
     # a B=16 capture scaled to B=64 by valid KV bytes
     "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh",
                "sha256": "bdbf5370ee5f9909a3c8113f1991ca09478653442bedf0c446fbd2db9b8c7ef8",
