@@ -317,7 +317,7 @@ def time_decode_fp8(gqa, name, device, flush, reps=20, warmup=3):
     lens = inp["cache_seqlens"].tolist()
     kv_bytes = roofline.decode_kv_bytes(w.Hkv, w.D, lens, elem_bytes=1)
     out = torch.empty_like(d["q"])
-    wsb = gqa.gqa_decode_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, 0, w.Smax)
+    wsb = gqa.gqa_decode_fp8_workspace_bytes(w.B, w.Hq, w.Hkv, w.D, 0, w.Smax)
     work = torch.empty((max(wsb, 16),), dtype=torch.uint8, device=device)
 
     def call():

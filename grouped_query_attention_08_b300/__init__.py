@@ -17,6 +17,8 @@ Functions keep the C names:
   gqa_decode_fp8(q, kcache, vcache, cache_seqlens, *, k_scale, v_scale, ...)
   gqa_decode_num_splits(B, Hkv, max_seqlen_k, num_splits)
   gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, max_seqlen_k)
+  gqa_decode_fp8_num_splits(B, Hkv, max_seqlen_k, num_splits)
+  gqa_decode_fp8_workspace_bytes(B, Hq, Hkv, D, num_splits, max_seqlen_k)
   gqa_device_status(stream=None)
   gqa_status_string(status)
 """
@@ -88,6 +90,10 @@ def load_library():
         lib.gqa_decode_num_splits.argtypes = [i32, i32, i32, i32]
         lib.gqa_decode_workspace_bytes.restype = sz
         lib.gqa_decode_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.gqa_decode_fp8_num_splits.restype = i32
+        lib.gqa_decode_fp8_num_splits.argtypes = [i32, i32, i32, i32]
+        lib.gqa_decode_fp8_workspace_bytes.restype = sz
+        lib.gqa_decode_fp8_workspace_bytes.argtypes = [i32, i32, i32, i32, i32, i32]
         lib.gqa_device_status.restype = i32
         lib.gqa_device_status.argtypes = [vp]
         lib.gqa_status_string.restype = ctypes.c_char_p
@@ -397,6 +403,18 @@ def gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, max_seqlen_k) -> int:
                                                          int(num_splits), int(max_seqlen_k)))
 
 
+def gqa_decode_fp8_num_splits(B, Hkv, max_seqlen_k, num_splits=0) -> int:
+    n = load_library().gqa_decode_fp8_num_splits(int(B), int(Hkv), int(max_seqlen_k), int(num_splits))
+    if n < 0:
+        raise GQAError(-n, "gqa_decode_fp8_num_splits")
+    return n
+
+
+def gqa_decode_fp8_workspace_bytes(B, Hq, Hkv, D, num_splits, max_seqlen_k) -> int:
+    return int(load_library().gqa_decode_fp8_workspace_bytes(int(B), int(Hq), int(Hkv), int(D),
+                                                             int(num_splits), int(max_seqlen_k)))
+
+
 def gqa_decode(q, kcache, vcache, cache_seqlens, *, scale=None, num_splits=0, out=None,
                workspace=None, stream=None):
     """Single-token decode.  q [B,Hq,D]; caches [B,Smax,Hkv,D]; cache_seqlens int32 [B].
@@ -418,7 +436,9 @@ def gqa_decode(q, kcache, vcache, cache_seqlens, *, scale=None, num_splits=0, ou
     _expect(out, q.shape, q.dtype, "out")
     if out is None:
         out = torch.empty_like(q)
-    need = gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, Smax)
+    dev = _check_cuda(q, kcache, vcache, cache_seqlens, out)
+    with _on(dev):      # the automatic split count depends on the device's SM count
+        need = gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, Smax)
     if workspace is None and need > 0:
         workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
     dev = _check_cuda(q, kcache, vcache, cache_seqlens, out, workspace)
@@ -458,7 +478,9 @@ def gqa_decode_fp8(q, kcache, vcache, cache_seqlens, k_scale, v_scale, *, scale=
     _expect(out, q.shape, q.dtype, "out")
     if out is None:
         out = torch.empty_like(q)
-    need = gqa_decode_workspace_bytes(B, Hq, Hkv, D, num_splits, Smax)
+    dev = _check_cuda(q, kcache, vcache, cache_seqlens, out)
+    with _on(dev):      # the automatic split count depends on the device's SM count
+        need = gqa_decode_fp8_workspace_bytes(B, Hq, Hkv, D, num_splits, Smax)
     if workspace is None and need > 0:
         workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
     dev = _check_cuda(q, kcache, vcache, cache_seqlens, out, workspace)

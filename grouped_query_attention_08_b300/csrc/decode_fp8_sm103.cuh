@@ -17,6 +17,13 @@
 //   out = sum p v_scale v8 / l = v_scale * (sum p v8 / l)
 // so k_scale folds into the softmax scale and v_scale into the output.
 //
+// CTA layout: one CTA per (split, group of kF8Warps K/V heads, b); warp w
+// streams head kF8Warps * group + w over every 16-key block of the split
+// through its own cp.async ring and writes that head's G output rows (or
+// split partials) itself, so no warps are merged.  A cached row holds the
+// Hkv heads side by side, so the CTA's warps read neighbouring 128-byte
+// pieces of each row rather than one piece per CTA.
+//
 // Matrix products run on mma.sync m16n8k16 in f16: every e4m3 value is
 // exact in f16 (cvt.rn.f16x2.e4m3x2), q is brought into f16's range by an
 // exact power-of-two scaling 2^e of the whole group (2^-e folds into the
@@ -31,6 +38,8 @@ namespace gqa {
 namespace decode {
 
 constexpr int kF8D = 128;
+constexpr int kF8Warps = 4;                 // warps per CTA = K/V heads per CTA
+constexpr int kF8Threads = kF8Warps * 32;
 
 struct ParamsF8 {
   const __nv_bfloat16* q;       // [B, Hq, 128]
@@ -49,11 +58,11 @@ struct ParamsF8 {
 // Per-warp ring of 16-key blocks, K rows then V rows, 128 bytes per row,
 // chunks XOR-swizzled with swz() as in the bf16 ring.
 struct RingF8 {
-  static constexpr int kRing = 4;                          // 3 blocks in flight per warp, 3 CTAs per SM
+  static constexpr int kRing = 4;                          // 3 blocks in flight per warp, 3 CTAs (64 KB) per SM
   static constexpr uint32_t kRowBytes = kF8D;
   static constexpr uint32_t kSlotBytes = 2 * kBlockKeys * kRowBytes;
   static constexpr uint32_t kWarpBytes = kRing * kSlotBytes;
-  static constexpr uint32_t kBytes = kWarps * kWarpBytes;
+  static constexpr uint32_t kBytes = kF8Warps * kWarpBytes;
 };
 
 // two e4m3 values (low byte, high byte) -> f16x2 (low half, high half)
@@ -148,21 +157,24 @@ DEVI void fetch_block_f8(BlockF8& R, uint32_t slot, int r, int c) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const ParamsF8 p) {
+__global__ void __launch_bounds__(kF8Threads) decode_split_fp8_kernel(const ParamsF8 p) {
   constexpr int D = kF8D;
   constexpr int KS = D / 16;      // k-steps of QK^T
   constexpr int MT = D / 16;      // m-tiles of O^T
   const int split = blockIdx.x;
-  const int kvh = blockIdx.y;
   const int b = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int r = lane >> 2;
   const int c = lane & 3;
+  // warp w streams K/V head kvh = kF8Warps * blockIdx.y + w: the CTA's warps
+  // read neighbouring 128-byte pieces of every cached row
+  const int kvh = kF8Warps * int(blockIdx.y) + warp;
+  if (kvh >= p.Hkv) return;
 
   int Lb = p.seqlens[b];
   if (Lb < 0 || Lb > p.Smax) {
-    if (split == 0 && kvh == 0 && threadIdx.x == 0) raise_error(kErrBounds);
+    if (split == 0 && kvh == 0 && lane == 0) raise_error(kErrBounds);
     Lb = 0;
   }
   const int kstart = split * p.split_len;
@@ -195,7 +207,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const Params
   };
 #pragma unroll
   for (int i = 0; i < RG::kRing - 1; ++i) {
-    const int bi = warp + i * kWarps;
+    const int bi = i;
     if (bi < nblk)
       issue(ring + uint32_t(i) * RG::kSlotBytes, kstart + bi * kBlockKeys);
     else
@@ -240,13 +252,13 @@ __global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const Params
 
   BlockF8 cur;
   int it = 0;
-  for (int blk = warp; blk < nblk; blk += kWarps, ++it) {
+  for (int blk = 0; blk < nblk; ++blk, ++it) {
     cp_async_wait<RG::kRing - 2>();
     __syncwarp();
     fetch_block_f8(cur, ring + uint32_t(it % RG::kRing) * RG::kSlotBytes, r, c);
     __syncwarp();
     {
-      const int nb = blk + (RG::kRing - 1) * kWarps;
+      const int nb = blk + (RG::kRing - 1);
       const uint32_t slot = ring + uint32_t((it + RG::kRing - 1) % RG::kRing) * RG::kSlotBytes;
       if (nb < nblk)
         issue(slot, kstart + nb * kBlockKeys);
@@ -280,22 +292,32 @@ __global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const Params
       xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, off));
       xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, off));
     }
-    const float nA = fmaxf(mA, xA), nB = fmaxf(mB, xB);
-    const float rA = (nA == -INFINITY) ? 0.f : nA, rB = (nB == -INFINITY) ? 0.f : nB;
-    const float aA = ex2_approx(mA - rA), aB = ex2_approx(mB - rB);
-    mA = nA;
-    mB = nB;
+    // The reference max of a head moves only when a block's max exceeds it by
+    // more than kRescaleThreshold (log2 units), so p <= 2^threshold and O, l
+    // are rescaled only then (a warp-uniform branch, rare after the first
+    // blocks); the merge through the log-sum-exp is exact for any reference.
+    const bool upA = xA > mA + kRescaleThreshold, upB = xB > mB + kRescaleThreshold;
+    if (__any_sync(0xffffffffu, upA || upB)) {
+      const float nA = upA ? xA : mA, nB = upB ? xB : mB;
+      const float aA = (mA == -INFINITY) ? 0.f : ex2_approx(mA - nA);
+      const float aB = (mB == -INFINITY) ? 0.f : ex2_approx(mB - nB);
+      mA = nA;
+      mB = nB;
+      lA *= aA;
+      lB *= aB;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= aA;
+        o[mt][1] *= aB;
+        o[mt][2] *= aA;
+        o[mt][3] *= aB;
+      }
+    }
+    const float rA = (mA == -INFINITY) ? 0.f : mA, rB = (mB == -INFINITY) ? 0.f : mB;
     const float pA0 = ex2_approx(tA0 - rA), pA1 = ex2_approx(tA1 - rA);
     const float pB0 = ex2_approx(tB0 - rB), pB1 = ex2_approx(tB1 - rB);
-    lA = lA * aA + pA0 + pA1;
-    lB = lB * aB + pB0 + pB1;
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      o[mt][0] *= aA;
-      o[mt][1] *= aB;
-      o[mt][2] *= aA;
-      o[mt][3] *= aB;
-    }
+    lA += pA0 + pA1;
+    lB += pB0 + pB1;
     const uint32_t pb0 = movmatrix_trans(pack_f16x2(pA0, pB0));
     const uint32_t pb1 = movmatrix_trans(pack_f16x2(pA1, pB1));
     // O^T += V^T . P^T: m-tile mt rows r / r+8 are dims 16 r + 2 mt (+1),
@@ -319,49 +341,35 @@ __global__ void __launch_bounds__(kThreads) decode_split_fp8_kernel(const Params
     lB += __shfl_xor_sync(0xffffffffu, lB, off);
   }
 
-  // ---- merge the 4 warps through shared memory (the rings are done)
-  __syncthreads();
-  float (*s_o)[8][D] = reinterpret_cast<float (*)[8][D]>(dsmem);
-  float (*s_m)[8] = reinterpret_cast<float (*)[8]>(dsmem + sizeof(float) * kWarps * 8 * D);
-  float (*s_l)[8] = reinterpret_cast<float (*)[8]>(dsmem + sizeof(float) * (kWarps * 8 * D + kWarps * 8));
+  // ---- this warp's G heads: lane (r, c) holds dims 16 r .. 16 r + 15 of
+  // heads 2c and 2c+1 (o[mt][0 / 2]: dims 16 r + 2 mt / +1 of head 2c,
+  // o[mt][1 / 3] of head 2c+1)
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt) {
-    const int d_lo = 16 * r + 2 * mt;
-    s_o[warp][2 * c][d_lo] = o[mt][0];
-    s_o[warp][2 * c + 1][d_lo] = o[mt][1];
-    s_o[warp][2 * c][d_lo + 1] = o[mt][2];
-    s_o[warp][2 * c + 1][d_lo + 1] = o[mt][3];
-  }
-  if (r == 0) {
-    s_m[warp][2 * c] = mA;
-    s_m[warp][2 * c + 1] = mB;
-    s_l[warp][2 * c] = lA;
-    s_l[warp][2 * c + 1] = lB;
-  }
-  __syncthreads();
-
-  const int G = p.G;
-  for (int idx = threadIdx.x; idx < G * D; idx += kThreads) {
-    const int n = idx / D, d = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_m[w][n]);
-    const float Mr = (M == -INFINITY) ? 0.f : M;
-    float num = 0.f, den = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      const float f = ex2_approx(s_m[w][n] - Mr);
-      num += f * s_o[w][n][d];
-      den += f * s_l[w][n];
-    }
-    const float val = den > 0.f ? num / den * p.v_scale : 0.f;
-    const size_t hrow = size_t(b) * p.Hq + size_t(kvh) * G + n;
+  for (int hh = 0; hh < 2; ++hh) {
+    const int n = 2 * c + hh;
+    if (n >= p.G) continue;
+    const float l = hh ? lB : lA;
+    const float m = hh ? mB : mA;
+    const float inv = l > 0.f ? p.v_scale / l : 0.f;
+    const size_t hrow = size_t(b) * p.Hq + size_t(kvh) * p.G + n;
     if (p.nsplit == 1) {
-      p.out[hrow * D + d] = __float2bfloat16_rn(val);
+      uint32_t w[8];
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) w[mt] = pack_bf16x2(o[mt][hh] * inv, o[mt][2 + hh] * inv);
+      uint4* dst = reinterpret_cast<uint4*>(p.out + hrow * D + 16 * r);
+      dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+      dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
     } else {
-      p.part_o[(hrow * p.nsplit + split) * D + d] = val;
-      if (d == 0)
-        p.part_lse[hrow * p.nsplit + split] = den > 0.f ? (Mr + log2f(den)) * 0.6931471805599453f : -INFINITY;
+      float4* dst = reinterpret_cast<float4*>(p.part_o + (hrow * p.nsplit + split) * D + 16 * r);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4)
+        dst[q4] = make_float4(o[2 * q4][hh] * inv, o[2 * q4][2 + hh] * inv, o[2 * q4 + 1][hh] * inv,
+                              o[2 * q4 + 1][2 + hh] * inv);
+      if (r == 0) {
+        float lg;
+        asm("lg2.approx.f32 %0, %1;" : "=f"(lg) : "f"(l));
+        p.part_lse[hrow * p.nsplit + split] = l > 0.f ? (m + lg) * 0.6931471805599453f : -INFINITY;
+      }
     }
   }
 }

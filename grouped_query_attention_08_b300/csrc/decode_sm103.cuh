@@ -39,6 +39,7 @@ namespace decode {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kBlockKeys = 16;
+constexpr float kRescaleThreshold = 8.0f;   // log2 units: p <= 2^8 (exact in bf16 and f16)
 
 struct Params {
   const __nv_bfloat16* q;       // [B, Hq, D]
@@ -252,22 +253,32 @@ __global__ void __launch_bounds__(kThreads)
       xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, off));
       xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, off));
     }
-    const float nA = fmaxf(mA, xA), nB = fmaxf(mB, xB);
-    const float rA = (nA == -INFINITY) ? 0.f : nA, rB = (nB == -INFINITY) ? 0.f : nB;
-    const float aA = ex2_approx(mA - rA), aB = ex2_approx(mB - rB);
-    mA = nA;
-    mB = nB;
+    // The reference max of a head moves only when a block's max exceeds it by
+    // more than kRescaleThreshold (log2 units), so p <= 2^threshold and O, l
+    // are rescaled only then (a warp-uniform branch, rare after the first
+    // blocks); the merge through the log-sum-exp is exact for any reference.
+    const bool upA = xA > mA + kRescaleThreshold, upB = xB > mB + kRescaleThreshold;
+    if (__any_sync(0xffffffffu, upA || upB)) {
+      const float nA = upA ? xA : mA, nB = upB ? xB : mB;
+      const float aA = (mA == -INFINITY) ? 0.f : ex2_approx(mA - nA);
+      const float aB = (mB == -INFINITY) ? 0.f : ex2_approx(mB - nB);
+      mA = nA;
+      mB = nB;
+      lA *= aA;
+      lB *= aB;
+#pragma unroll
+      for (int mt = 0; mt < MT; ++mt) {
+        o[mt][0] *= aA;
+        o[mt][1] *= aB;
+        o[mt][2] *= aA;
+        o[mt][3] *= aB;
+      }
+    }
+    const float rA = (mA == -INFINITY) ? 0.f : mA, rB = (mB == -INFINITY) ? 0.f : mB;
     const float pA0 = ex2_approx(tA0 - rA), pA1 = ex2_approx(tA1 - rA);
     const float pB0 = ex2_approx(tB0 - rB), pB1 = ex2_approx(tB1 - rB);
-    lA = lA * aA + pA0 + pA1;
-    lB = lB * aB + pB0 + pB1;
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt) {
-      o[mt][0] *= aA;
-      o[mt][1] *= aB;
-      o[mt][2] *= aA;
-      o[mt][3] *= aB;
-    }
+    lA += pA0 + pA1;
+    lB += pB0 + pB1;
     // P^T fragments: transpose the two 8x8 (key x head) halves of P
     const uint32_t pb0 = movmatrix_trans(pack_bf16x2(pA0, pB0));
     const uint32_t pb1 = movmatrix_trans(pack_bf16x2(pA1, pB1));
@@ -357,12 +368,27 @@ __global__ void __launch_bounds__(128)
   const int wib = threadIdx.x >> 5;
   const int row = blockIdx.x * 4 + wib;
   const int lane = threadIdx.x & 31;
+  // Launched as a programmatic dependent of the split kernel: this grid may
+  // start while the split kernel's last CTAs run, and waits here until that
+  // grid has completed and its partials are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   if (row >= B * Hq) return;
   const int b = row / Hq;
   int Lb = seqlens[b];
   if (Lb < 0 || Lb > Smax) Lb = 0;
   const int nvalid = min(min(nsplit, kCombineMaxSplits), (Lb + split_len - 1) / split_len);
   const float* lrow = part_lse + size_t(row) * nsplit;
+  const float* orow = part_o + size_t(row) * nsplit * D;
+  // The first kPre splits' partials are loaded before the weights are known,
+  // so that their latency overlaps that of the lse values.
+  constexpr int kPre = VEC > 1 ? 16 : 1;
+  using V = typename std::conditional<VEC == 4, float4, float2>::type;
+  V pre[kPre];
+  if constexpr (VEC > 1) {
+#pragma unroll
+    for (int s = 0; s < kPre; ++s)
+      if (s < nvalid) pre[s] = __ldcs(reinterpret_cast<const V*>(orow + size_t(s) * D) + lane);
+  }
   float M = -INFINITY;
   for (int s = lane; s < nvalid; s += 32) M = fmaxf(M, lrow[s]);
 #pragma unroll
@@ -378,15 +404,26 @@ __global__ void __launch_bounds__(128)
   for (int off = 16; off > 0; off >>= 1) W += __shfl_xor_sync(0xffffffffu, W, off);
   __syncwarp();
   const float inv = W > 0.f ? 1.f / W : 0.f;
-  const float* orow = part_o + size_t(row) * nsplit * D;
   if constexpr (VEC > 1) {
     // D == 32 * VEC: lane owns d = VEC*lane .. VEC*lane + VEC-1
-    using V = typename std::conditional<VEC == 4, float4, float2>::type;
     float acc[VEC];
 #pragma unroll
     for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int s = 0; s < kPre; ++s) {
+      if (s < nvalid) {
+        const V x = pre[s];
+        const float w = s_w[wib][s];
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
+        if constexpr (VEC == 4) {
+          acc[2] += w * x.z;
+          acc[3] += w * x.w;
+        }
+      }
+    }
 #pragma unroll 8
-    for (int s = 0; s < nvalid; ++s) {
+    for (int s = kPre; s < nvalid; ++s) {
       const V x = __ldcs(reinterpret_cast<const V*>(orow + size_t(s) * D) + lane);
       const float w = s_w[wib][s];
       acc[0] += w * x.x;

@@ -244,8 +244,6 @@ bool decode_fp8_smem_attr_set(int dev) {
   if (dev >= 0 && dev < kMaxDevices) done[dev] = true;
   return true;
 }
-static_assert(gqa::decode::RingF8::kBytes >= sizeof(float) * (gqa::decode::kWarps * 8 * 128 + 2 * gqa::decode::kWarps * 8),
-              "the fp8 decode merge reuses the ring memory");
 
 template <int D>
 bool bwd_smem_attr_set(int dev) {
@@ -312,14 +310,19 @@ struct SplitPlan {
 
 // n requested (<= 0: automatic) -> split length rounded up to 16 keys; the
 // launched count is ceil(Smax / len) so that no split is empty for a full cache.
-SplitPlan plan_splits(int B, int Hkv, int Smax, int num_splits) {
+// Automatic: about target_len keys per split, and enough CTAs (B * ceil(Hkv /
+// heads_per_cta) per split) for several waves.  The bf16 / fp32 split kernel
+// takes 1024 keys of one K/V head per CTA; the FP8 kernel, whose CTAs stream
+// four K/V heads at half the bytes per key, 512 keys (measured on B300 for
+// llama_decode_fp8: 512 keys per split 0.126 ms, 1024 keys 0.139 ms).
+SplitPlan plan_splits(int B, int Hkv, int Smax, int num_splits, int target_len = 1024, int heads_per_cta = 1) {
   int n = num_splits;
   if (n <= 0) {
-    // automatic: about 1024 keys per split, and enough CTAs for several waves
     const int sms = num_sms(current_device());
-    n = (Smax + 1023) / 1024;
+    n = (Smax + target_len - 1) / target_len;
     const long long want = 4LL * sms;
-    while ((long long)n * B * Hkv < want && n < kMaxSplits && (Smax + n) / (n + 1) >= 256) ++n;
+    const long long groups = (long long)B * ((Hkv + heads_per_cta - 1) / heads_per_cta);
+    while ((long long)n * groups < want && n < kMaxSplits && (Smax + n) / (n + 1) >= 256) ++n;
   }
   n = std::max(1, std::min(n, kMaxSplits));
   const int blocks = (Smax + 15) / 16;
@@ -332,6 +335,10 @@ SplitPlan plan_splits(int B, int Hkv, int Smax, int num_splits) {
   return sp;
 }
 
+SplitPlan plan_splits_fp8(int B, int Hkv, int Smax, int num_splits) {
+  return plan_splits(B, Hkv, Smax, num_splits, 512, gqa::decode::kF8Warps);
+}
+
 size_t workspace_for(int B, int Hq, int D, int n) {
   if (n <= 1) return 0;
   const size_t o = size_t(B) * Hq * n * D * sizeof(float);
@@ -339,7 +346,29 @@ size_t workspace_for(int B, int Hq, int D, int n) {
   return ((o + 255) / 256) * 256 + l;
 }
 
+// The split-KV combine, launched as a programmatic dependent of the split
+// kernel just queued on the same stream: its launch overlaps the split
+// kernel's tail, and griddepcontrol.wait inside it orders the reads of the
+// partials after that grid has completed.
+template <typename OutT, int VEC>
+cudaError_t launch_combine(cudaStream_t st, const float* part_o, const float* part_lse, const int* seqlens, OutT* out,
+                           int B, int Hq, int D, int nsplit, int split_len, int Smax) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned((B * Hq + 3) / 4));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gqa::decode::combine_kernel<OutT, VEC>, part_o, part_lse, seqlens, out, B, Hq, D,
+                            nsplit, split_len, Smax);
+}
+
 }  // namespace
+
 
 // ====================================================================== ABI
 extern "C" {
@@ -606,7 +635,7 @@ int gqa_decode_fp8(const void* q, const void* kcache, const void* vcache, const 
   const int G = Hq / Hkv;
   if (D != gqa::decode::kF8D || G > 8) return GQA_ERR_UNSUPPORTED;
   if (B > 65535 || Hkv > 65535) return GQA_ERR_UNSUPPORTED;
-  const SplitPlan sp = plan_splits(B, Hkv, max_seqlen_k, num_splits);
+  const SplitPlan sp = plan_splits_fp8(B, Hkv, max_seqlen_k, num_splits);
   const size_t need = workspace_for(B, Hq, D, sp.n);
   if (need > 0 && (!workspace || workspace_bytes < need || !aligned(workspace, 16))) return GQA_ERR_INVALID_ARG;
   float* part_o = static_cast<float*>(workspace);
@@ -632,15 +661,13 @@ int gqa_decode_fp8(const void* q, const void* kcache, const void* vcache, const 
   p.scale_k_log2 = float(double(scale) * double(k_scale) * 1.4426950408889634);
   p.v_scale = v_scale;
   if (!decode_fp8_smem_attr_set(current_device())) return GQA_ERR_CUDA;
-  gqa::decode::decode_split_fp8_kernel<<<dim3(sp.n, Hkv, B), gqa::decode::kThreads, gqa::decode::RingF8::kBytes,
+  gqa::decode::decode_split_fp8_kernel<<<dim3(sp.n, (Hkv + gqa::decode::kF8Warps - 1) / gqa::decode::kF8Warps, B),
+                                         gqa::decode::kF8Threads, gqa::decode::RingF8::kBytes,
                                          st>>>(p);
   if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
-  if (sp.n > 1) {
-    const int rows = B * Hq;
-    gqa::decode::combine_kernel<__nv_bfloat16, 4><<<(rows + 3) / 4, 128, 0, st>>>(
-        part_o, part_lse, cache_seqlens, static_cast<__nv_bfloat16*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
-    if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
-  }
+  if (sp.n > 1 && launch_combine<__nv_bfloat16, 4>(st, part_o, part_lse, cache_seqlens, static_cast<__nv_bfloat16*>(out),
+                                                    B, Hq, D, sp.n, sp.len, max_seqlen_k) != cudaSuccess)
+    return GQA_ERR_CUDA;
   return GQA_OK;
 }
 
@@ -713,6 +740,17 @@ size_t gqa_decode_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits,
   return workspace_for(B, Hq, D, plan_splits(B, Hkv, max_seqlen_k, num_splits).n);
 }
 
+int gqa_decode_fp8_num_splits(int B, int Hkv, int max_seqlen_k, int num_splits) {
+  if (B <= 0 || Hkv <= 0 || max_seqlen_k <= 0) return -GQA_ERR_INVALID_ARG;
+  if (num_splits > kMaxSplits) return -GQA_ERR_INVALID_ARG;
+  return plan_splits_fp8(B, Hkv, max_seqlen_k, num_splits).n;
+}
+
+size_t gqa_decode_fp8_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits, int max_seqlen_k) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || max_seqlen_k <= 0 || num_splits > kMaxSplits) return 0;
+  return workspace_for(B, Hq, D, plan_splits_fp8(B, Hkv, max_seqlen_k, num_splits).n);
+}
+
 int gqa_decode(const void* q, const void* kcache, const void* vcache, const int* cache_seqlens, void* out, int B,
                int Hq, int Hkv, int D, float scale, int num_splits, int max_seqlen_k, int dtype, void* workspace,
                size_t workspace_bytes, void* stream) {
@@ -758,14 +796,13 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
       gqa::decode::decode_split_kernel<128><<<grid, gqa::decode::kThreads, decode_smem_bytes<128>(), st>>>(p);
     if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
     if (sp.n > 1) {
-      const int rows = B * Hq;
-      if (D == 128)
-        gqa::decode::combine_kernel<__nv_bfloat16, 4><<<(rows + 3) / 4, 128, 0, st>>>(
-            part_o, part_lse, cache_seqlens, static_cast<__nv_bfloat16*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
-      else
-        gqa::decode::combine_kernel<__nv_bfloat16, 2><<<(rows + 3) / 4, 128, 0, st>>>(
-            part_o, part_lse, cache_seqlens, static_cast<__nv_bfloat16*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
-      if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+      __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
+      const cudaError_t e =
+          D == 128 ? launch_combine<__nv_bfloat16, 4>(st, part_o, part_lse, cache_seqlens, ob, B, Hq, D, sp.n, sp.len,
+                                                      max_seqlen_k)
+                   : launch_combine<__nv_bfloat16, 2>(st, part_o, part_lse, cache_seqlens, ob, B, Hq, D, sp.n, sp.len,
+                                                      max_seqlen_k);
+      if (e != cudaSuccess) return GQA_ERR_CUDA;
     }
     return GQA_OK;
   }
@@ -802,12 +839,9 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache, const int*
     p.len_cap = max_seqlen_k;
     const int rc = launch_f32(p, st);
     if (rc != GQA_OK) return rc;
-    if (sp.n > 1) {
-      const int rows = B * Hq;
-      gqa::decode::combine_kernel<float, 1><<<(rows + 3) / 4, 128, 0, st>>>(
-          part_o, part_lse, cache_seqlens, static_cast<float*>(out), B, Hq, D, sp.n, sp.len, max_seqlen_k);
-      if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
-    }
+    if (sp.n > 1 && launch_combine<float, 1>(st, part_o, part_lse, cache_seqlens, static_cast<float*>(out), B, Hq, D,
+                                             sp.n, sp.len, max_seqlen_k) != cudaSuccess)
+      return GQA_ERR_CUDA;
     return GQA_OK;
   }
   return GQA_ERR_INVALID_ARG;

@@ -319,8 +319,10 @@ int gqa_decode(const void* q, const void* kcache, const void* vcache,
  *                  k_scale * kcache and the value v_scale * vcache (the
  *                  caller quantises x as round(x / scale) to e4m3)
  *   everything else as gqa_decode (bf16 out, cache_seqlens, scale,
- *   num_splits, max_seqlen_k, workspace of gqa_decode_workspace_bytes(B,
- *   Hq, Hkv, 128, num_splits, max_seqlen_k) bytes).
+ *   num_splits, max_seqlen_k), except that the split count is
+ *   gqa_decode_fp8_num_splits(...) and the workspace needs
+ *   gqa_decode_fp8_workspace_bytes(B, Hq, Hkv, 128, num_splits,
+ *   max_seqlen_k) bytes.
  * Result: gqa_decode's definition on the dequantised cache.  D must be 128
  * and G <= 8 (GQA_ERR_UNSUPPORTED otherwise); q/out/caches 16-byte aligned;
  * scale, k_scale and v_scale finite (GQA_ERR_INVALID_ARG otherwise).
@@ -329,6 +331,19 @@ int gqa_decode_fp8(const void* q, const void* kcache, const void* vcache,
                    const int* cache_seqlens, void* out, int B, int Hq, int Hkv, int D,
                    float scale, float k_scale, float v_scale, int num_splits, int max_seqlen_k,
                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gqa_decode_fp8_num_splits / gqa_decode_fp8_workspace_bytes -- the split
+ * count and workspace size of gqa_decode_fp8, with the same arguments,
+ * clamping, return values and errors as gqa_decode_num_splits /
+ * gqa_decode_workspace_bytes.  Only the automatic choice (num_splits <= 0)
+ * differs: about 512 keys per split instead of 1024, because each FP8 CTA
+ * streams four K/V heads at half the bytes per key.  No page defines these
+ * calls: they size the caller-owned workspace of the FP8 split step.
+ */
+int gqa_decode_fp8_num_splits(int B, int Hkv, int max_seqlen_k, int num_splits);
+size_t gqa_decode_fp8_workspace_bytes(int B, int Hq, int Hkv, int D, int num_splits,
+                                      int max_seqlen_k);
 
 /*
  * gqa_decode_noalloc -- gqa_decode for callers that cannot allocate device

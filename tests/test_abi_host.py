@@ -165,6 +165,22 @@ def test_split_planning(lib):
     assert ws >= 64 * 64 * 8 * 129 * 4
 
 
+def test_fp8_split_planning(lib):
+    # explicit counts plan exactly as the bf16 decode's
+    for args in ((4, 8, 8192, 1), (4, 8, 8192, 8), (4, 8, 100, 3), (4, 8, 100, 7), (4, 8, 40, 100)):
+        assert gqa.gqa_decode_fp8_num_splits(*args) == gqa.gqa_decode_num_splits(*args)
+        B, Hkv, smax, ns = args
+        assert (gqa.gqa_decode_fp8_workspace_bytes(B, 4 * Hkv, Hkv, 128, ns, smax)
+                == gqa.gqa_decode_workspace_bytes(B, 4 * Hkv, Hkv, 128, ns, smax))
+    # automatic: about 512 keys per split (148 SMs when no GPU is present)
+    n8 = gqa.gqa_decode_fp8_num_splits(64, 8, 8192, 0)
+    assert n8 == 16 and gqa.gqa_decode_num_splits(64, 8, 8192, 0) == 8
+    assert gqa.gqa_decode_fp8_workspace_bytes(64, 64, 8, 128, 0, 8192) >= 64 * 64 * 16 * 129 * 4
+    with pytest.raises(gqa.GQAError):
+        gqa.gqa_decode_fp8_num_splits(64, 8, 8192, 129)
+    assert gqa.gqa_decode_fp8_workspace_bytes(0, 64, 8, 128, 0, 8192) == 0
+
+
 def _dec8(lib, B=2, Hq=8, Hkv=2, D=128, scale=0.1, ks=0.01, vs=0.02, ns=1, smax=64, ws=None, wsb=0, q=FAKE,
           kc=FAKE, lens=FAKE):
     P = ctypes.c_void_p

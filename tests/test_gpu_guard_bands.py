@@ -148,7 +148,7 @@ def test_fp8_decode_writes_stay_inside_out_and_workspace(ns):
     B, Hq, Hkv, D, Smax = 3, 16, 2, 128, 301
     d = to_dev(inputs.make_decode_fp8(B, Hq, Hkv, D, Smax, seed=17, lens=(0, Smax)))
     out = Guarded(d["q"].shape, d["q"].dtype)
-    wsb = gqa.gqa_decode_workspace_bytes(B, Hq, Hkv, D, ns, Smax)
+    wsb = gqa.gqa_decode_fp8_workspace_bytes(B, Hq, Hkv, D, ns, Smax)
     work = Guarded((max(wsb, 16),), torch.uint8)
     gqa.gqa_decode_fp8(d["q"], d["kcache"], d["vcache"], d["cache_seqlens"], d["k_scale"], d["v_scale"],
                        num_splits=ns, out=out.t, workspace=work.t)
