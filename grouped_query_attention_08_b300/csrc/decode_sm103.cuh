@@ -374,29 +374,32 @@ __global__ void __launch_bounds__(128)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (row >= B * Hq) return;
   const int b = row / Hq;
-  int Lb = seqlens[b];
-  if (Lb < 0 || Lb > Smax) Lb = 0;
-  const int nvalid = min(min(nsplit, kCombineMaxSplits), (Lb + split_len - 1) / split_len);
   const float* lrow = part_lse + size_t(row) * nsplit;
   const float* orow = part_o + size_t(row) * nsplit * D;
-  // The first kPre splits' partials are loaded before the weights are known,
-  // so that their latency overlaps that of the lse values.
+  // Every load is issued before the key length (and with it the number of
+  // splits that were written) is known, so that all their latencies overlap:
+  // the first 32 splits' lse and the first kPre splits' partials.  Splits past
+  // the sequence hold stale workspace values, which get no weight below.
+  const float lse0 = lane < nsplit ? __ldcs(lrow + lane) : -INFINITY;
   constexpr int kPre = VEC > 1 ? 16 : 1;
   using V = typename std::conditional<VEC == 4, float4, float2>::type;
   V pre[kPre];
   if constexpr (VEC > 1) {
 #pragma unroll
     for (int s = 0; s < kPre; ++s)
-      if (s < nvalid) pre[s] = __ldcs(reinterpret_cast<const V*>(orow + size_t(s) * D) + lane);
+      if (s < nsplit) pre[s] = __ldcs(reinterpret_cast<const V*>(orow + size_t(s) * D) + lane);
   }
+  int Lb = seqlens[b];
+  if (Lb < 0 || Lb > Smax) Lb = 0;
+  const int nvalid = min(min(nsplit, kCombineMaxSplits), (Lb + split_len - 1) / split_len);
   float M = -INFINITY;
-  for (int s = lane; s < nvalid; s += 32) M = fmaxf(M, lrow[s]);
+  for (int s = lane; s < nvalid; s += 32) M = fmaxf(M, s < 32 ? lse0 : lrow[s]);
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
   const float Mr = (M == -INFINITY) ? 0.f : M;
   float W = 0.f;
   for (int s = lane; s < nvalid; s += 32) {
-    const float e = expf(lrow[s] - Mr);
+    const float e = expf((s < 32 ? lse0 : lrow[s]) - Mr);
     s_w[wib][s] = e;
     W += e;
   }
