@@ -50,8 +50,8 @@ NCU_TRAFFIC = {
                 "workload": "bert_base", "bytes": 94322432},
     # a B=16 capture scaled to B=64 by valid KV bytes
     "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh",
-               "sha256": "bdbf5370ee5f9909a3c8113f1991ca09478653442bedf0c446fbd2db9b8c7ef8",
-               "workload": "llama_decode", "bytes": 1275700000},
+               "sha256": "3da23f2311d8b3f1dad3c2a6686fd96218f2aa4cc6d53874bd51a4448f128b40",
+               "workload": "llama_decode", "bytes": 1271529128},
 }
 
 

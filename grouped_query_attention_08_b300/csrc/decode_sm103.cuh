@@ -103,8 +103,19 @@ struct Ring {
 
 DEVI uint32_t swz(int row) { return uint32_t((((row >> 1) & 3) << 1) ^ ((row & 1) << 2)); }
 
+// L2 policy for the cached K/V rows: each is read exactly once, so they are
+// marked first to be evicted, which keeps the split partials (written during
+// the kernel and read back by the combine) and q in L2 while gigabytes of
+// cache stream through it.
+DEVI uint64_t policy_evict_first() {
+  uint64_t p;
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 DEVI void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src), "r"(src_bytes),
+               "l"(policy_evict_first())
+               : "memory");
 }
 DEVI void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
