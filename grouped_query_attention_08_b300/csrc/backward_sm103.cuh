@@ -16,7 +16,7 @@
 //   dQ_i = scale sum_j dS_ij k_j,   dK_j = scale sum_{h in group, i} dS_ij q_i
 // Three kernels, no atomics, so the result does not depend on scheduling:
 //  * dsum_kernel: Dsum per query row.
-//  * dq_kernel, persistent (one CTA per SM looping over tiles), a tile being
+//  * dq_kernel, persistent (one CTA per SM claiming tiles), a tile being
 //    Mq tokens x G heads of K/V head kvh = 128 rows (row = token * G +
 //    head-in-group, as in the forward): per 128-key tile S = Q K^T and
 //    dP = dO V^T into TMEM, dS = P (dP - Dsum) written back as packed bf16,
@@ -71,6 +71,10 @@ struct Params {
   // waits on its abort barrier, which nothing arrives on yet, so the wait runs
   // out after timeout_ns and the CTA takes its abort path.
   int test_stall;
+  // dq_kernel's tile scheduler of this launch: sched[0] counts tiles claimed
+  // past the first gridDim.x, sched[1] CTAs that finished; the last CTA to
+  // finish sets both back to zero for the next launch that uses the slot.
+  unsigned int* sched;
 };
 
 // Key length of batch entry b (a bad length raises a device error and
@@ -170,9 +174,12 @@ struct DqLayout {
   static constexpr uint32_t kOffK = 2 * kTileBytes;
   static constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
   static constexpr uint32_t kOffBar = kOffV + kStages * kTileBytes;
-  // q_full, kv_full[S], kv_empty[S], s_full, p_full, done, drain, sd_read, dq_done, q_empty, dq_free
-  static constexpr int kNumBars = 1 + 2 * kStages + 8;
-  static constexpr uint32_t kOffSlot = kOffBar + 8u * kNumBars;
+  // q_full, kv_full[S], kv_empty[S], s_full, p_full, done, drain, sd_read, dq_done, q_empty, dq_free,
+  // tq_full[kTQ], tq_empty[kTQ]
+  static constexpr int kTQ = 4;                            // tile-queue entries
+  static constexpr int kNumBars = 1 + 2 * kStages + 8 + 2 * kTQ;
+  static constexpr uint32_t kOffTQ = kOffBar + 8u * kNumBars;   // [kTQ] int: claimed tile indices
+  static constexpr uint32_t kOffSlot = kOffTQ + 4u * kTQ;
   static constexpr uint32_t kOffAbort = kOffSlot + 8u;
   static constexpr uint32_t kBytes = kOffAbort + 8u;
   static constexpr uint32_t kSmemAlloc = kBytes + 1024u;
@@ -221,9 +228,11 @@ struct KvLayout {
   static_assert(kSmemAlloc > 116u * 1024u, "one CTA per SM: its TMEM allocation takes all 512 columns");
 };
 
-// dQ, persistent: CTA c takes tiles c, c + gridDim.x, ... of the
-// n_qt * Hkv * B tiles (tile = Mq tokens x G heads of K/V head kvh, batch b;
-// the token block varies fastest, so neighbouring CTAs share K/V in L2).
+// dQ, persistent: CTA c takes tile c first, then claims tiles from a
+// counter in global memory (dynamic scheduling: it runs beside dkdv_kernel,
+// whose CTAs leave SMs at different times), out of the n_qt * Hkv * B tiles
+// (tile = Mq tokens x G heads of K/V head kvh, batch b; the token block varies
+// fastest, so CTAs running at one time share K/V in L2).
 // Iteration counters run on across tiles, so the next tile's Q/dO and K/V
 // land while the current one is computed.  Schedule over a tile's key tiles
 // j (one issuing thread: the tensor core runs its MMAs in issue order):
@@ -254,6 +263,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t s_full = bar(1 + 2 * S), p_full = bar(2 + 2 * S), done = bar(3 + 2 * S), drain = bar(4 + 2 * S);
   const uint32_t sd_read = bar(5 + 2 * S), dq_done = bar(6 + 2 * S);
   const uint32_t q_empty = bar(7 + 2 * S), dq_free = bar(8 + 2 * S);
+  auto tq_full = [&](int i) { return bar(9 + 2 * S + i); };
+  auto tq_empty = [&](int i) { return bar(9 + 2 * S + L::kTQ + i); };
+  volatile int* tq = reinterpret_cast<volatile int*>(sbase + L::kOffTQ);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sbase + L::kOffAbort);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sbase + L::kOffSlot);
   const uint64_t to = p.timeout_ns;
@@ -277,6 +289,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     T.n = kmax > 0 ? (kmax + kBN - 1) / kBN : 0;
     return T;
   };
+  // Tiles are claimed at run time: the producer publishes this CTA's kq-th
+  // tile (blockIdx.x first, then claims from the launch's counter, one tile
+  // ahead) in queue entry kq % kTQ; n_tiles or more ends the loops.  A warp
+  // (elementwise) releases the entry with one arrival once every lane has
+  // read it; the MMA thread arrives itself.
+  auto next_tile = [&](int kq, bool& okq, bool whole_warp) -> int {
+    const int qi = kq % L::kTQ;
+    okq = mbar_wait(tq_full(qi), (kq / L::kTQ) & 1, abort_flag, p.timeout_ns);
+    const int t = okq ? tq[qi] : n_tiles;
+    if (whole_warp) {
+      __syncwarp();
+      if ((threadIdx.x & 31) == 0) mbar_arrive(tq_empty(qi));
+    } else {
+      mbar_arrive(tq_empty(qi));
+    }
+    return t;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
@@ -292,6 +321,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(sd_read, kEwWarps);
     mbar_init(dq_done, 1);
     mbar_init(dq_free, kEwWarps);
+    for (int i = 0; i < L::kTQ; ++i) {
+      mbar_init(tq_full(i), 1);
+      mbar_init(tq_empty(i), 1 + kEwWarps);   // the MMA thread and one arrival per elementwise warp
+    }
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -318,7 +351,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int g = 0;                  // K/V tiles loaded so far (ring position)
       int k = 0;                  // tiles with work so far (Q/dO buffer phase)
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      int t_next = int(blockIdx.x);
+      for (int kq = 0; ok; ++kq) {
+        const int t = t_next;
+        const int qi = kq % L::kTQ;
+        ok = mbar_wait(tq_empty(qi), ((kq / L::kTQ) & 1) ^ 1, abort_flag, to);
+        if (!ok) break;
+        if (t < n_tiles) {
+          unsigned int v;
+          asm volatile("atom.global.add.u32 %0, [%1], 1;" : "=r"(v) : "l"(p.sched) : "memory");
+          t_next = int(gridDim.x + v);
+        }
+        tq[qi] = t;
+        mbar_arrive(tq_full(qi));   // release: the entry is visible to the consumers
+        if (t >= n_tiles) break;
         const Tile T = tile_info(t);
         if (T.n == 0) continue;
         // the Q/dO buffer is free once the previous tile's copies into TMEM are done
@@ -375,7 +421,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = !p.test_stall || mbar_wait(drain, 0, abort_flag, to);
       int g = 0;                  // key-tile iterations so far (all tiles)
       int k = 0;                  // tiles with work so far
-      for (int t = blockIdx.x; ok && t < n_tiles; t += gridDim.x) {
+      for (int kq = 0; ok; ++kq) {
+        const int t = next_tile(kq, ok, false);
+        if (!ok || t >= n_tiles) break;
         const int n = tile_info(t).n;
         if (n == 0) continue;
         ok = mbar_wait(q_full, k & 1, abort_flag, to) && mbar_wait(kv_full(g % S), (g / S) & 1, abort_flag, to);
@@ -448,7 +496,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool aborted = false;
     int g = 0;                    // key-tile iterations so far (all tiles)
     int k = 0;                    // tiles with work so far
-    for (int t = blockIdx.x; !aborted && t < n_tiles; t += gridDim.x) {
+    for (int kq = 0; !aborted; ++kq) {
+      bool okq;
+      const int t = next_tile(kq, okq, true);
+      if (!__all_sync(0xffffffffu, okq)) {
+        aborted = true;
+        break;
+      }
+      if (t >= n_tiles) break;
       const Tile T = tile_info(t);
       const int i = T.q0 + token;
       const bool row_ok = r < p.G * p.Mq && i < p.Sq;
@@ -552,6 +607,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kWarpMMA) {
     tc_fence_after();
     tmem_dealloc(tmem, L::kTmCols);
+  }
+  if (threadIdx.x == 0) {
+    // every claim of this CTA is done: count it out; the last CTA resets the
+    // scheduler slot for the next launch that uses it
+    __threadfence();
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
+    }
   }
 }
 

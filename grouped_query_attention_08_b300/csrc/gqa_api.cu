@@ -81,7 +81,7 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Work-unit scheduler slots of the prefill kernel: each launch takes the next
+// Work-unit scheduler slots of the prefill and dQ kernels: each launch takes the next
 // slot (a claim counter and a finished-CTA counter); the launch's last CTA
 // puts the slot back to zero.  Launches that use one slot must not overlap on
 // the GPU, which holds unless kSchedSlots launches are in flight at once.
@@ -260,6 +260,18 @@ bool bwd_smem_attr_set(int dev) {
 }
 
 // Dsum, then dQ and dK/dV (independent of each other) on one stream.
+// Side stream of the backward, per device: dK/dV runs on it beside dQ, so
+// that its CTAs take the SMs that dQ's persistent CTAs leave as they finish
+// (and dQ's last CTAs run beside dK/dV's last wave) instead of the two
+// kernels each ending on a partly idle GPU.
+struct BwdAux {
+  bool ready = false;
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+std::mutex g_bwd_aux_mu;
+BwdAux g_bwd_aux[kMaxDevices];
+
 // q, out, dout [B, Sq, Hq, D]; k, v [B, Sk, Hkv, D] (bf16).
 template <int D>
 int launch_bwd(gqa::bwd::Params p, const void* q, const void* k, const void* v, cudaStream_t stream) {
@@ -289,10 +301,34 @@ int launch_bwd(gqa::bwd::Params p, const void* q, const void* k, const void* v, 
   const long long dq_tiles = (long long)p.n_qt * p.Hkv * p.B;
   if (dq_tiles > 0x7fffffffLL) return GQA_ERR_UNSUPPORTED;
   const unsigned gq = unsigned(std::min<long long>(dq_tiles, num_sms(current_device())));
-  bw::dq_kernel<D><<<gq, bw::kThreads, bw::DqLayout<D>::kSmemAlloc, stream>>>(tmQg, tmDOg, tmK, tmV, p);
   const dim3 gk(unsigned(p.n_kt), unsigned(p.Hkv), unsigned(p.B));
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return GQA_ERR_CUDA;
+  p.sched = sched_slot(dev);
+  if (!p.sched) return GQA_ERR_CUDA;
+  // Fork after Dsum: dK/dV on the caller's stream, launched first, and dQ on
+  // the side stream: its persistent CTAs take SMs as dK/dV's CTAs leave them
+  // and claim tiles as they go, so the last partial wave of dK/dV and dQ's
+  // work share the GPU.  The caller's stream then waits for both.  The lock
+  // keeps the record / wait pairs of concurrent callers apart (the events
+  // are shared).
+  std::lock_guard<std::mutex> lock(g_bwd_aux_mu);
+  BwdAux& ax = g_bwd_aux[dev];
+  if (!ax.ready) {
+    if (cudaStreamCreateWithFlags(&ax.st, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ax.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ax.join, cudaEventDisableTiming) != cudaSuccess)
+      return GQA_ERR_CUDA;
+    ax.ready = true;
+  }
+  if (cudaEventRecord(ax.fork, stream) != cudaSuccess || cudaStreamWaitEvent(ax.st, ax.fork, 0) != cudaSuccess)
+    return GQA_ERR_CUDA;
   bw::dkdv_kernel<D><<<gk, bw::kThreads, bw::KvLayout<D>::kSmemAlloc, stream>>>(tmK, tmV, tmQ1, tmDO1, p);
-  return cudaGetLastError() == cudaSuccess ? GQA_OK : GQA_ERR_CUDA;
+  bw::dq_kernel<D><<<gq, bw::kThreads, bw::DqLayout<D>::kSmemAlloc, ax.st>>>(tmQg, tmDOg, tmK, tmV, p);
+  if (cudaGetLastError() != cudaSuccess) return GQA_ERR_CUDA;
+  if (cudaEventRecord(ax.join, ax.st) != cudaSuccess || cudaStreamWaitEvent(stream, ax.join, 0) != cudaSuccess)
+    return GQA_ERR_CUDA;
+  return GQA_OK;
 }
 
 int launch_f32(const gqa::f32::Params& p, cudaStream_t stream) {
