@@ -70,9 +70,9 @@ constexpr int kWarpTMA = 8;
 constexpr int kWarpMMA = 9;      // issues the MMAs of Q tile 0
 constexpr int kWarpMMA2 = 10;    // issues the MMAs of Q tile 1
 constexpr int kThreads = 384;
-constexpr int kSoftmaxRegs = 216;   // 2 x 128 x 216 + 128 x 72 = 384 x 168 registers at launch
+constexpr int kSoftmaxRegs = 224;   // 2 x 128 x 224 + 128 x 56 = 384 x 168 registers at launch
 constexpr int kLaunchRegs = 168;
-constexpr int kOtherRegs = 72;
+constexpr int kOtherRegs = 56;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kUQ = 4;                // depth of the shared-memory work-unit queue
 // consumers of a queue entry: the two MMA-issuing threads and every softmax
