@@ -75,6 +75,7 @@ constexpr int kLaunchRegs = 168;
 constexpr int kOtherRegs = 56;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr int kUQ = 4;                // depth of the shared-memory work-unit queue
+constexpr int kMaxLptB = 64;          // batch entries up to which units are claimed longest first
 // consumers of a queue entry: the two MMA-issuing threads and every softmax
 // warp (one elected arrival per warp)
 constexpr uint32_t kUQConsumers = kNQT + kNQT * 4;
@@ -106,7 +107,8 @@ struct Layout {
   static constexpr uint32_t kOffUQ = kOffBar + 8u * kNumBars;
   static constexpr uint32_t kOffTmemSlot = kOffUQ + 32u * kUQ;
   static constexpr uint32_t kOffAbort = kOffTmemSlot + 8u;
-  static constexpr uint32_t kBytes = kOffAbort + 8u;
+  static constexpr uint32_t kOffOrd = kOffAbort + 8u;         // [kMaxLptB] batch entries, longest first
+  static constexpr uint32_t kBytes = kOffOrd + 4u * kMaxLptB;
   static constexpr uint32_t kSmemAlloc = kBytes + 1024u;    // slack to align the base to 1024 B
   // V is the MN-major B operand: 8-key groups 1024 B apart (SBO); the second
   // 64-wide head-dim half (D = 128) is kHalfBytes further (LBO).  With D = 64
@@ -466,17 +468,51 @@ __global__ void __launch_bounds__(kThreads, 1)
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
   if (warp == kWarpTMA) {
     // ------------------------------------------------------------ producer
+    // Non-causal launches whose entries have their own key lengths (dense
+    // with seqlens, or packed) and B <= kMaxLptB hand out units longest
+    // first: batch entries in order of decreasing key length (ties by index),
+    // all units of an entry together, so the units left at the end of the
+    // launch are the shortest and the last SMs to finish wait least.  The warp
+    // ranks the B lengths: lane b counts the entries that sort before entry b.
+    int* ord = reinterpret_cast<int*>(sbase + L::kOffOrd);
+    const bool lpt = !kSparse && !p.causal && (kPacked || p.seqlens != nullptr) && p.B <= kMaxLptB;
+    auto key_len_of = [&](int bb) -> int {
+      if constexpr (kPacked) return ldg_nc_i32(p.cu_k + bb + 1) - ldg_nc_i32(p.cu_k + bb);
+      return ldg_nc_i32(p.seqlens + bb);
+    };
+    if (lpt) {
+      const int L0 = lane < p.B ? key_len_of(lane) : 0;
+      const int L1 = lane + 32 < p.B ? key_len_of(lane + 32) : 0;
+      int r0 = 0, r1 = 0;
+      for (int b2 = 0; b2 < p.B; ++b2) {
+        const int Lx = __shfl_sync(0xffffffffu, b2 < 32 ? L0 : L1, b2 & 31);
+        r0 += (Lx > L0 || (Lx == L0 && b2 < lane)) ? 1 : 0;
+        r1 += (Lx > L1 || (Lx == L1 && b2 < lane + 32)) ? 1 : 0;
+      }
+      if (lane < p.B) ord[r0] = lane;
+      if (lane + 32 < p.B) ord[r1] = lane + 32;
+      __syncwarp();
+    }
+    // claim index c -> unit index (the identity unless longest first)
+    auto unit_of = [&](int c) -> int {
+      if (!lpt || c >= p.n_units) return c;
+      const int per_b = p.n_qblk * p.Hkv;
+      const int bi = c / per_b, rem = c - bi * per_b;
+      const int qidx = rem / p.Hkv, kvh = rem - qidx * p.Hkv;
+      return qidx * (p.B * p.Hkv) + ord[bi] * p.Hkv + kvh;
+    };
     if (lane == 0) {
       uint32_t kv_it = 0;       // K/V tiles issued so far (ring position)
       uint32_t qn = 0;          // units with work so far (Q buffer position)
       bool ok = true;
       bool k_only = false;
       const uint32_t q_bytes = uint32_t(kNQT * L::kHalves * 64 * 2 * rows_per_tile);
-      // Work units are claimed at run time (the first one is blockIdx.x; the
-      // grid never exceeds the unit count), one unit ahead, and published to
-      // the MMA and softmax warps through the unit queue; a unit index past
-      // the last unit ends every role's loop.
-      int u_next = int(blockIdx.x);
+      // Work units are claimed at run time (the first claim index is
+      // blockIdx.x; the grid never exceeds the unit count), one unit ahead,
+      // mapped to a unit by unit_of and published to the MMA and softmax
+      // warps through the unit queue; a unit index past the last unit ends
+      // every role's loop.
+      int u_next = unit_of(int(blockIdx.x));
       for (uint32_t k = 0; ok; ++k) {
         const int u = u_next;
         const int i = int(k % kUQ);
@@ -492,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             sq.act_hi = uint32_t(act >> 32);
           }
         }
-        if (u < p.n_units) u_next = claim_unit(p);
+        if (u < p.n_units) u_next = unit_of(claim_unit(p));
         uq[8 * i] = u;
         uq[8 * i + 1] = sq.Lk;
         uq[8 * i + 2] = sq.Lq;
