@@ -22,6 +22,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -400,6 +401,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--warmup-seconds", type=float, default=1.5,
                     help="minimum wall time of back-to-back warm-up steps right before the timed steps")
+    ap.add_argument("--min-timed-ms", type=float, default=250.0,
+                    help="each timed step repeats the pass (flush, prefill, decode) R times, R chosen from "
+                         "the warm-up so that the K steps take at least this long")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--prefill", default="bert_base",
                     choices=["bert_base", "bert_large_long", "causal_long"])
@@ -473,7 +477,6 @@ def main():
         raise RuntimeError("device error in the first step")
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clocks:
         # Warm-up inside the clock sampler and right before the timed steps:
@@ -489,41 +492,51 @@ def main():
             torch.cuda.synchronize()
         if gqa.gqa_device_status() != 0:
             raise RuntimeError("device error during warm-up")
+        # Inner repetitions: every timed step runs the pass R times, so that
+        # the K steps (exactly K, as asked) take at least --min-timed-ms even
+        # when K is small; R comes from the warm-up's wall time per pass and is
+        # the same on every rank (the largest).
+        pass_ms = (time.perf_counter() - t0) * 1e3 / max(1, n_warm)
+        R = max(1, math.ceil(args.min_timed_ms / (K * pass_ms))) if args.min_timed_ms > 0 else 1
+        R = int(_max_over_ranks(float(R), ws, device))
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K * R)]
         _barrier(ws)
         torch.cuda.synchronize()
         t_start.record()
         for i in range(K):
-            flush.fill_(i & 0xFF)
-            ev[i][0].record()
-            prefill()
-            ev[i][1].record()
-            decode()
-            ev[i][2].record()
+            for rr in range(R):
+                j = i * R + rr
+                flush.fill_(j & 0xFF)
+                ev[j][0].record()
+                prefill()
+                ev[j][1].record()
+                decode()
+                ev[j][2].record()
         t_end.record()
         torch.cuda.synchronize()
         _barrier(ws)
     clk = clocks.summary()
     if gqa.gqa_device_status() != 0:
         raise RuntimeError("device error in the timed region")
-    t_pre = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
-    t_dec = [ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]
+    t_pre = [e[0].elapsed_time(e[1]) for e in ev]     # every pass (K * R)
+    t_dec = [e[1].elapsed_time(e[2]) for e in ev]
     total_ms = t_start.elapsed_time(t_end)
     pre_s = _max_over_ranks(sum(t_pre) / 1e3, ws, device)
     dec_s = _max_over_ranks(sum(t_dec) / 1e3, ws, device)
     total_s = _max_over_ranks(total_ms / 1e3, ws, device)
 
-    # per-step distribution (this rank): median and min beside the mean
-    per_step = {"prefill_ms": {"mean": statistics.fmean(t_pre), "median": statistics.median(t_pre),
+    # per-pass distribution (this rank): median and min beside the mean
+    per_step = {"inner_reps": R, "passes": K * R, "prefill_ms": {"mean": statistics.fmean(t_pre), "median": statistics.median(t_pre),
                                "min": min(t_pre), "max": max(t_pre)},
                 "decode_ms": {"mean": statistics.fmean(t_dec), "median": statistics.median(t_dec),
                               "min": min(t_dec), "max": max(t_dec)},
                 "warmup_steps_run": n_warm, "timed_region_ms": total_ms}
 
-    value = _whole_job_rate(flops_p, K, ws, pre_s) / 1e12
-    dec_gbs = _whole_job_rate(kv_bytes_d, K, ws, dec_s) / 1e9
+    value = _whole_job_rate(flops_p, K * R, ws, pre_s) / 1e12
+    dec_gbs = _whole_job_rate(kv_bytes_d, K * R, ws, dec_s) / 1e9
     peaks, psrc = _peaks()
-    pre_avg = pre_s / K
-    dec_avg = dec_s / K
+    pre_avg = pre_s / (K * R)
+    dec_avg = dec_s / (K * R)
     pre_ach = flops_p / pre_avg / 1e12
     dec_ach = bytes_d / dec_avg / 1e9
     tr_p, tr_d = _traffic("prefill"), _traffic("decode")
@@ -619,14 +632,16 @@ def main():
                 "parallelism": "replicas" if ws > 1 else "single GPU",
                 "prefill_ms": pre_avg * 1e3, "decode_ms": dec_avg * 1e3, "decode_num_splits": nsplit,
                 "warmup": "%d steps and >= %.1f s of back-to-back steps inside the clock sampler, "
-                          "immediately before the timed steps" % (args.warmup, args.warmup_seconds)},
+                          "immediately before the timed steps" % (args.warmup, args.warmup_seconds),
+                "step": "%d passes (L2 flush, prefill, decode) per timed step, so that the %d steps take "
+                        ">= %.0f ms; prefill_ms / decode_ms are per pass" % (R, K, args.min_timed_ms)},
             "per_step": per_step,
             "roofline": roof_p,
             "decode": {"value": dec_gbs, "unit": "GB/s (KV-cache bytes read / decode time)",
                        "roofline": roof_d, "kv_bytes_per_step": kv_bytes_d},
             "clocks": clk,
             "e2e": e2e,
-            "gpu_launches": launches_per_step * K,
+            "gpu_launches": launches_per_step * K * R,
             "cpu_baseline": cb,
             "prefill_workloads": others,
             "decode_fp8": dec8,
