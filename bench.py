@@ -47,8 +47,8 @@ PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 NCU_TRAFFIC = {
     # one launch on bert_base
     "prefill": {"source": "grouped_query_attention_08_b300/csrc/prefill_sm103.cuh",
-                "sha256": "5cc4f8841ac12ade15ed0f9f1520581132fd7ef85d5156ddb8f96d0cedc888e9",
-                "workload": "bert_base", "bytes": 94322432},
+                "sha256": "66cde4ea4676e13ce3cc2f3449d42839bb4c0aee1f7be5fe558b7cf635d72e8c",
+                "workload": "bert_base", "bytes": 88589824},
     # a B=16 capture scaled to B=64 by valid KV bytes
     "decode": {"source": "grouped_query_attention_08_b300/csrc/decode_sm103.cuh",
                "sha256": "3da23f2311d8b3f1dad3c2a6686fd96218f2aa4cc6d53874bd51a4448f128b40",
