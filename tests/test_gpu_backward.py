@@ -121,6 +121,27 @@ def test_bwd_is_deterministic_and_zero_past_the_key_length():
         assert torch.all(a[1][bi, L:] == 0) and torch.all(a[2][bi, L:] == 0)
 
 
+def test_bwd_scheduler_slots_and_side_stream_across_many_calls():
+    """dQ claims its tiles from a per-launch counter slot (shared with the
+    prefill's, 64 slots reset by each launch's last CTA) and runs on a side
+    stream beside dK/dV: 70 backward calls interleaved with prefill calls
+    reuse every slot and must keep giving bitwise the first gradients, on
+    the caller's stream order (each call's outputs read back on it)."""
+    inp = inputs.make_backward(2, 12, 3, 300, 300, 64, seed=8, lens=(90, 300))
+    out, lse = _oracle_fwd(inp, 0.125, False)
+    first = _run(inp, out, lse, 0.125, False)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    o_d, l_d = out.cuda(), lse.cuda()
+    for i in range(70):
+        got = gqa.gqa_bwd(d["q"], d["k"], d["v"], o_d, d["dout"], l_d, seqlens_k=d["seqlens_k"], scale=0.125)
+        gqa.gqa_fwd(d["q"], d["k"], d["v"], seqlens_k=d["seqlens_k"], scale=0.125)
+        if i % 10 == 9:
+            for x, y in zip(got, first):
+                assert torch.equal(x, y), i
+    torch.cuda.synchronize()
+    assert gqa.gqa_device_status() == 0
+
+
 def _full_size(name, seed):
     """The named workload at full size through the library's forward and
     backward, as bench.py times it; dO ~ N(0,1) from `seed`."""
