@@ -243,7 +243,10 @@ int gqa_fwd_sparse(const void* q, const void* k, const void* v, void* out, float
  * gives up raises GQA_ERR_DEVICE_TIMEOUT.  Gradients accumulate in fp32; P
  * and dS are rounded to bf16 for the products.  No atomics: the result does
  * not depend on scheduling.  Buffers must not overlap.  Launches three
- * kernels on `stream` and returns without synchronising.
+ * kernels and returns without synchronising: Dsum and dK/dV on `stream`, dQ
+ * on a side stream the library keeps per device, forked from `stream` after
+ * Dsum and joined back to it by events, so every output is ready in
+ * `stream` order (and a stream capture records both branches).
  */
 int gqa_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
             const float* lse, float* dsum, void* dq, void* dk, void* dv, int B, int Hq, int Hkv,
